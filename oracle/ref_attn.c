@@ -1,0 +1,275 @@
+/*
+ * Plain fp64 CPU oracle for exact scaled-dot-product attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
+ * calls this file; only the test suite, the smoke check and the CPU-baseline
+ * leg of the benchmark do.  It shares no code, header or table with the CUDA
+ * path.
+ *
+ * What it computes is the plain definition of attention that the pages say
+ * the tiled method reproduces exactly ("exata, identica matematicamente a
+ * versao padrao"):
+ *
+ *   S = tau * Q K^T                      (scaled scores, one row per query)
+ *   P = softmax_row(S)  over the visible keys J(i)
+ *   O = P V
+ *   LSE_i = m_i + ln l_i,  m_i = max_j S_ij,  l_i = sum_j exp(S_ij - m_i)
+ *
+ * Sources (page title, section):
+ *   - tonho.wtf "flash attention" encyclopedia entry, section "como funciona":
+ *     the scores tau*Q_i K_j^T, the per-row running max m and sum l, and that
+ *     the output and the statistics (m, l) are what is stored.
+ *   - same page, section "como funciona", backward paragraph: the backward
+ *     keeps only O and (m, l), rebuilds S and P, and uses D_i = P_i . dP_i,
+ *     which equals dO_i . O_i.
+ *   - "Atencao eficiente - FlashAttention, sparse e hibrida", section
+ *     "Insight 2 - Online softmax": the blocked softmax is identical to the
+ *     softmax over the whole row.
+ *
+ * Readings where the pages are silent:
+ *   - causal: key j is visible from query i iff j <= i (equal query and key
+ *     lengths, so top-left and bottom-right alignment coincide);
+ *   - LSE is in natural-log units of the tau-scaled scores;
+ *   - the backward is the analytic gradient of O with respect to Q, K, V for
+ *     an upstream gradient dO, with the softmax Jacobian written out as
+ *     dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik).
+ *
+ * Layout: every tensor is a contiguous array [BH][N][d] of doubles (row-major,
+ * d fastest); LSE and D are [BH][N].  BH is batch * heads.
+ *
+ * No blocking, fusion or reordering: each query row is done on its own, in
+ * the order of the definition above.  OpenMP only splits independent rows
+ * or heads across threads.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Key j is visible from query i. */
+static int visible(int64_t i, int64_t j, int causal)
+{
+    return !causal || j <= i;
+}
+
+static double dot(const double* a, const double* b, int64_t d)
+{
+    double s = 0.0;
+    for (int64_t k = 0; k < d; ++k) s += a[k] * b[k];
+    return s;
+}
+
+/*
+ * One query row of the forward pass.
+ *   q     : the query row (d values)
+ *   K, V  : the keys and values of this head ([N][d])
+ *   i     : the query's position (for the causal mask)
+ *   p     : scratch of N doubles; on return p[j] = P_ij (0 for hidden keys)
+ *   o     : d outputs, O_i = sum_j P_ij V_j
+ *   lse   : m + ln l
+ */
+static void row_forward(const double* q, const double* K, const double* V,
+                        int64_t i, int64_t N, int64_t d, double tau, int causal,
+                        double* p, double* o, double* lse)
+{
+    double m = -INFINITY;
+    for (int64_t j = 0; j < N; ++j) {
+        if (visible(i, j, causal)) {
+            p[j] = tau * dot(q, K + j * d, d);
+            if (p[j] > m) m = p[j];
+        }
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        if (visible(i, j, causal)) {
+            p[j] = exp(p[j] - m);
+            l += p[j];
+        } else {
+            p[j] = 0.0;
+        }
+    }
+    for (int64_t j = 0; j < N; ++j) p[j] /= l;
+    for (int64_t k = 0; k < d; ++k) o[k] = 0.0;
+    for (int64_t j = 0; j < N; ++j) {
+        if (p[j] == 0.0) continue;
+        const double* v = V + j * d;
+        for (int64_t k = 0; k < d; ++k) o[k] += p[j] * v[k];
+    }
+    *lse = m + log(l);
+}
+
+/* Number of threads a parallel region of this library uses. */
+int ora_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void ora_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/*
+ * The attention probabilities P [BH][N][N] (row i is the softmax of the
+ * visible scaled scores of query i; hidden keys get 0).  For small checks.
+ */
+void ora_attn_probs(const double* Q, const double* K, const double* V,
+                    int64_t BH, int64_t N, int64_t d, double tau, int causal,
+                    double* P)
+{
+    int64_t rows = BH * N;
+#pragma omp parallel
+    {
+        double* o = (double*)malloc(sizeof(double) * (size_t)(d > 0 ? d : 1));
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < rows; ++r) {
+            int64_t bh = r / N, i = r % N;
+            double lse;
+            row_forward(Q + r * d, K + bh * N * d, V + bh * N * d, i, N, d, tau,
+                        causal, P + r * N, o, &lse);
+        }
+        free(o);
+    }
+}
+
+/* Forward pass over every row: O [BH][N][d], LSE [BH][N]. */
+void ora_attn_fwd(const double* Q, const double* K, const double* V,
+                  int64_t BH, int64_t N, int64_t d, double tau, int causal,
+                  double* O, double* LSE)
+{
+    int64_t rows = BH * N;
+#pragma omp parallel
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < rows; ++r) {
+            int64_t bh = r / N, i = r % N;
+            row_forward(Q + r * d, K + bh * N * d, V + bh * N * d, i, N, d, tau,
+                        causal, p, O + r * d, LSE + r);
+        }
+        free(p);
+    }
+}
+
+/*
+ * Forward pass on a chosen set of rows.  rows[k] = bh * N + i names query i of
+ * head bh; outputs O_rows [nrows][d] and LSE_rows [nrows] in the same order.
+ */
+void ora_attn_fwd_rows(const double* Q, const double* K, const double* V,
+                       int64_t BH, int64_t N, int64_t d, double tau, int causal,
+                       const int64_t* rows, int64_t nrows,
+                       double* O_rows, double* LSE_rows)
+{
+    (void)BH;
+#pragma omp parallel
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t k = 0; k < nrows; ++k) {
+            int64_t r = rows[k];
+            int64_t bh = r / N, i = r % N;
+            row_forward(Q + r * d, K + bh * N * d, V + bh * N * d, i, N, d, tau,
+                        causal, p, O_rows + k * d, LSE_rows + k);
+        }
+        free(p);
+    }
+}
+
+/*
+ * Backward pass: the gradients of O = softmax(tau Q K^T) V with respect to
+ * Q, K and V for an upstream gradient dO, per head:
+ *
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . V_j
+ *   D_i   = sum_j P_ij dP_ij          (softmax Jacobian term)
+ *   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = tau sum_j dS_ij K_j
+ *   dK_j  = tau sum_i dS_ij Q_i
+ *
+ * P is recomputed here from Q and K (the oracle's own fp64 forward).  O_out,
+ * LSE_out and D_out are optional extra outputs (pass NULL to skip); D_out is
+ * the softmax-Jacobian row sum above, so a test can hold it against dO_i . O_i.
+ */
+void ora_attn_bwd(const double* Q, const double* K, const double* V,
+                  const double* dO,
+                  int64_t BH, int64_t N, int64_t d, double tau, int causal,
+                  double* dQ, double* dK, double* dV,
+                  double* O_out, double* LSE_out, double* D_out)
+{
+#pragma omp parallel
+    {
+        double* P = (double*)malloc(sizeof(double) * (size_t)(N * N));
+        double* dS = (double*)malloc(sizeof(double) * (size_t)(N * N));
+        double* o = (double*)malloc(sizeof(double) * (size_t)(d > 0 ? d : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t bh = 0; bh < BH; ++bh) {
+            const double* Qh = Q + bh * N * d;
+            const double* Kh = K + bh * N * d;
+            const double* Vh = V + bh * N * d;
+            const double* dOh = dO + bh * N * d;
+            double* dQh = dQ + bh * N * d;
+            double* dKh = dK + bh * N * d;
+            double* dVh = dV + bh * N * d;
+
+            /* forward: P and (optionally) O, LSE */
+            for (int64_t i = 0; i < N; ++i) {
+                double lse;
+                row_forward(Qh + i * d, Kh, Vh, i, N, d, tau, causal,
+                            P + i * N, o, &lse);
+                if (O_out) memcpy(O_out + (bh * N + i) * d, o, sizeof(double) * (size_t)d);
+                if (LSE_out) LSE_out[bh * N + i] = lse;
+            }
+            /* dP, D and dS, row by row */
+            for (int64_t i = 0; i < N; ++i) {
+                double* dSi = dS + i * N;
+                const double* Pi = P + i * N;
+                double Di = 0.0;
+                for (int64_t j = 0; j < N; ++j) {
+                    dSi[j] = visible(i, j, causal) ? dot(dOh + i * d, Vh + j * d, d) : 0.0;
+                    Di += Pi[j] * dSi[j];
+                }
+                for (int64_t j = 0; j < N; ++j) dSi[j] = Pi[j] * (dSi[j] - Di);
+                if (D_out) D_out[bh * N + i] = Di;
+            }
+            /* dQ_i = tau sum_j dS_ij K_j */
+            for (int64_t i = 0; i < N; ++i) {
+                double* g = dQh + i * d;
+                for (int64_t k = 0; k < d; ++k) g[k] = 0.0;
+                for (int64_t j = 0; j < N; ++j) {
+                    double w = dS[i * N + j];
+                    if (w == 0.0) continue;
+                    for (int64_t k = 0; k < d; ++k) g[k] += w * Kh[j * d + k];
+                }
+                for (int64_t k = 0; k < d; ++k) g[k] *= tau;
+            }
+            /* dK_j = tau sum_i dS_ij Q_i ;  dV_j = sum_i P_ij dO_i */
+            for (int64_t j = 0; j < N; ++j) {
+                double* gk = dKh + j * d;
+                double* gv = dVh + j * d;
+                for (int64_t k = 0; k < d; ++k) { gk[k] = 0.0; gv[k] = 0.0; }
+                for (int64_t i = 0; i < N; ++i) {
+                    double ws = dS[i * N + j], wp = P[i * N + j];
+                    if (ws != 0.0)
+                        for (int64_t k = 0; k < d; ++k) gk[k] += ws * Qh[i * d + k];
+                    if (wp != 0.0)
+                        for (int64_t k = 0; k < d; ++k) gv[k] += wp * dOh[i * d + k];
+                }
+                for (int64_t k = 0; k < d; ++k) gk[k] *= tau;
+            }
+        }
+        free(P);
+        free(dS);
+        free(o);
+    }
+}
