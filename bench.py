@@ -1,0 +1,458 @@
+#!/usr/bin/env python
+"""Throughput of exact IO-aware attention (forward + backward) on GB300.
+
+One step = one forward (fa_fwd) and one backward (fa_bwd) over one batch of
+the long-context workload: B=1, H=16, N=16384, d=128, causal, bf16 inputs
+(seeded synthetic N(0,1) data with a sink key row, as in the workload table).
+Counted FLOPs: 4*B*H*N^2*d forward, x2.5 backward, halved for causal.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  N > 1 runs N independent replicas (one per
+GPU, launched by torchrun); the path has no exchange step, so there is no
+data-path collective, only a barrier and a max over ranks for timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("attention fwd and fwd+bwd TFLOP/s (bf16, causal) and % of GB300 dense BF16 peak")
+DEFAULT_WORKLOAD = "long_sink_b1h16_n16384_d128_causal"
+L2_FLUSH_BYTES = 512 << 20          # > the 129 MB L2, written between timed steps
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+# --------------------------------------------------------------- helpers ----
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world: int, device=None):
+    import torch.distributed as dist
+    if world > 1:
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of a float over ranks (identity at world size 1)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(flops_per_step: float, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job TFLOP/s: every rank ran `steps` replica steps; the job took the
+    slowest rank's time."""
+    return world * steps * flops_per_step / max_seconds / 1e12
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_io_aware_12_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            doc = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if doc.get("source_hash") != kernel_source_hash():
+        return None
+    ent = doc.get("kernels", {}).get(kernel)
+    return None if ent is None else ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    def __init__(self, index: int, period_ms: int = 100):
+        self.index, self.period_ms, self.proc, self.path = index, period_ms, None, None
+
+    def __enter__(self):
+        out_dir = os.path.join(ROOT, "gpurun_out")
+        os.makedirs(out_dir, exist_ok=True)
+        self.path = os.path.join(out_dir, f"clocks_gpu{self.index}.csv")
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period_ms}"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, power, reasons = [], None, [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["unsampled"]}
+        # "under load": samples drawing at least half the peak power seen
+        pmax = max(power) if power else 0.0
+        loaded = [s for s, p in zip(sm, power) if p >= 0.5 * pmax] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": pmax}
+
+
+def pick_workload(args):
+    """The named workload, or (--shape B,H,N,d,causal) a same-recipe variant
+    used for profiling captures of a smaller case."""
+    from exact_io_aware_12_gb300.workloads import BY_NAME, Workload
+    w = BY_NAME[args.workload]
+    if args.shape:
+        B, H, N, d, c = (int(v) for v in args.shape.split(","))
+        w = Workload(f"{w.name}@{B}x{H}x{N}x{d}{'c' if c else ''}", B, H, N, d, bool(c), w.seed,
+                     w.qk_scale, w.sink)
+    return w
+
+
+# ------------------------------------------------------------ our impl ----
+def run_ours(args):
+    import torch
+    from exact_io_aware_12_gb300 import api, _lib
+    from exact_io_aware_12_gb300.workloads import flops_fwd, flops_bwd, make_inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    if rank == 0:
+        _lib.load()               # builds if needed, once
+    barrier(world, dev)
+    _lib.load()
+
+    w = pick_workload(args)
+    B, H, N, d = w.shape
+    f_fwd = flops_fwd(B, H, N, d, w.causal)
+    f_bwd = flops_bwd(B, H, N, d, w.causal)
+    f_step = f_fwd + f_bwd
+    x = make_inputs(w)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(api.workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        api.fwd(q, k, v, w.causal, w.tau, out=o, lse=lse)
+        api.bwd(q, k, v, o, do, lse, w.causal, w.tau, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize(dev)
+    if api.last_device_error(dev) != _lib.FA_OK:
+        raise RuntimeError("kernel watchdog fired during warm-up")
+
+    # events: whole step, forward kernel, backward main kernel (per step)
+    st_s, st_e = [ev() for _ in range(args.steps)], [ev() for _ in range(args.steps)]
+    kf_s, kf_e = [ev() for _ in range(args.steps)], [ev() for _ in range(args.steps)]
+    kb_s, kb_e = [ev() for _ in range(args.steps)], [ev() for _ in range(args.steps)]
+    for e in st_s + st_e + kf_s + kf_e + kb_s + kb_e:
+        e.record(stream)           # materialise the handles
+    torch.cuda.synchronize(dev)
+
+    with ClockSampler(local) as clocks:
+        barrier(world, dev)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))                      # L2 flush, outside the step events
+            st_s[i].record(stream)
+            _lib.check(_lib.fa_set_timing_events(kf_s[i].cuda_event, kf_e[i].cuda_event), "timing")
+            api.fwd(q, k, v, w.causal, w.tau, out=o, lse=lse)
+            _lib.check(_lib.fa_set_timing_events(kb_s[i].cuda_event, kb_e[i].cuda_event), "timing")
+            api.bwd(q, k, v, o, do, lse, w.causal, w.tau, dq=dq, dk=dk, dv=dv, workspace=ws)
+            _lib.check(_lib.fa_set_timing_events(None, None), "timing")
+            st_e[i].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world, dev)
+        wall = time.perf_counter() - t0
+    if api.last_device_error(dev) != _lib.FA_OK:
+        raise RuntimeError("kernel watchdog fired during the timed steps")
+
+    step_ms = [a.elapsed_time(b) for a, b in zip(st_s, st_e)]
+    fwd_ms = [a.elapsed_time(b) for a, b in zip(kf_s, kf_e)]
+    bwd_ms = [a.elapsed_time(b) for a, b in zip(kb_s, kb_e)]
+    total_s = reduce_max(sum(step_ms) / 1e3, world, dev)
+    value = aggregate_value(f_step, args.steps, world, total_s)
+    fwd_avg = reduce_max(sum(fwd_ms) / len(fwd_ms), world, dev)
+    bwd_avg = reduce_max(sum(bwd_ms) / len(bwd_ms), world, dev)
+
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    fwd_tf = f_fwd / (fwd_avg / 1e3) / 1e12
+    bwdk_tf = f_bwd / (bwd_avg / 1e3) / 1e12
+    step_avg_ms = total_s * 1e3 / args.steps
+    # the dominant kernel by device time
+    if bwd_avg >= fwd_avg:
+        dom, dom_tf, dom_name = "fa_bwd_main_kernel", bwdk_tf, "bwd_main"
+    else:
+        dom, dom_tf, dom_name = "fa_fwd_kernel", fwd_tf, "fwd"
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(dom_tf, 2),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(dom_tf / peak, 4),
+                "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
+                "traffic": profiled_traffic(dom_name)}
+
+    e2e = run_e2e(args, w, x, dev, f_step) if not args.no_e2e else None
+    cpu = run_cpu_baseline(w, budget_s=args.cpu_seconds) if (rank == 0 and not args.no_cpu) else None
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_avg_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, key row 0 = 4 x mean query per head)",
+        "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
+                   "step": "fa_fwd + fa_bwd", "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed before every timed step (512 MiB write, outside the step events)"},
+        "frac_of_peak": round(value / world / peak, 4),
+        "fwd": {"ms": round(fwd_avg, 4), "tflops": round(fwd_tf, 2), "frac": round(fwd_tf / peak, 4)},
+        "bwd_main_kernel": {"ms": round(bwd_avg, 4), "tflops": round(bwdk_tf, 2),
+                            "frac": round(bwdk_tf / peak, 4)},
+        "fwd_bwd_step": {"ms": round(step_avg_ms, 4), "tflops_per_gpu": round(value / world, 2)},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed_loop": round(wall, 3),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, x, dev, f_step):
+    """Same step through the public API with host buffers: pinned host inputs
+    copied in, outputs (O, LSE, dQ, dK, dV) copied back, inside the timing."""
+    import torch
+    from exact_io_aware_12_gb300 import api
+
+    world, _, _ = dist_env()
+    B, H, N, d = w.shape
+    hin = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
+    dq_, dk_, dv_, o_ = (torch.empty(w.shape, dtype=torch.bfloat16).pin_memory() for _ in range(4))
+    lse_ = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    din = {n: torch.empty_like(hin[n], device=dev) for n in hin}
+    ws = torch.empty(api.workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for n in din:
+            din[n].copy_(hin[n], non_blocking=True)
+        o, lse = api.fwd(din["q"], din["k"], din["v"], w.causal, w.tau)
+        dq, dk, dv = api.bwd(din["q"], din["k"], din["v"], o, din["do"], lse, w.causal, w.tau,
+                             workspace=ws)
+        for src, dst in ((o, o_), (lse, lse_), (dq, dq_), (dk, dk_), (dv, dv_)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world, dev)
+    s.record(stream)
+    for _ in range(args.steps):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    t = reduce_max(s.elapsed_time(e) / 1e3, world, dev)
+    h2d = sum(t_.numel() * t_.element_size() for t_ in hin.values())
+    d2h = sum(t_.numel() * t_.element_size() for t_ in (o_, lse_, dq_, dk_, dv_))
+    return {"value": round(aggregate_value(f_step, args.steps, world, t), 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(t * 1e3 / args.steps, 4)}
+
+
+# ------------------------------------------------------------ CPU oracle ----
+def oracle_sample(w, budget_s: float):
+    """Times the fp64 oracle on a bounded sample of the workload: the forward on
+    sampled query rows of every head and the backward on a causal prefix.
+    Returns (flops, seconds, description)."""
+    import numpy as np
+    import oracle
+    from exact_io_aware_12_gb300.workloads import flops_fwd, flops_bwd, make_inputs
+
+    x = make_inputs(w)
+    B, H, N, d = w.shape
+    q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
+    # calibrate: a few rows, then size the sample to ~budget/2 for each half
+    rng = np.random.default_rng(7)
+    probe_rows = (np.arange(B * H) * N)[:, None] + rng.integers(0, N, size=(B * H, 2))
+    t0 = time.perf_counter()
+    oracle.fwd_rows(q, k, v, w.tau, w.causal, probe_rows.ravel())
+    t_probe = time.perf_counter() - t0
+    f_probe = sum(4.0 * d * ((r % N) + 1 if w.causal else N) for r in probe_rows.ravel())
+    rate = f_probe / max(t_probe, 1e-6)
+    per_row = 4.0 * d * (N / 2 if w.causal else N)
+    n_rows = int(max(B * H, min(B * H * N, (budget_s / 2) * rate / per_row)))
+    per_head = max(1, n_rows // (B * H))
+    rows = ((np.arange(B * H) * N)[:, None] + rng.integers(0, N, size=(B * H, per_head))).ravel()
+    t0 = time.perf_counter()
+    oracle.fwd_rows(q, k, v, w.tau, w.causal, rows)
+    t_f = time.perf_counter() - t0
+    f_f = sum(4.0 * d * ((r % N) + 1 if w.causal else N) for r in rows)
+    # backward on a prefix sized to the other half of the budget
+    n_b = 64
+    while n_b * 2 <= N and flops_bwd(B, H, n_b * 2, d, w.causal) / rate * 3 < budget_s / 2:
+        n_b *= 2
+    sl = lambda a: np.ascontiguousarray(a[:, :, :n_b])
+    t0 = time.perf_counter()
+    oracle.bwd(sl(q), sl(k), sl(v), sl(do), w.tau, w.causal)
+    t_b = time.perf_counter() - t0
+    f_b = flops_bwd(B, H, n_b, d, w.causal)
+    desc = (f"forward on {rows.size} random query rows ({per_head}/head) + backward on the "
+            f"{n_b}-token causal prefix, all {B * H} heads; FLOPs counted as on the GPU")
+    return f_f + f_b, t_f + t_b, desc
+
+
+def run_cpu_baseline(w, budget_s: float):
+    import oracle
+    flops, secs, desc = oracle_sample(w, budget_s)
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: rank 0 only, host cores."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    w = pick_workload(args)
+    per_step = max(1.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step)
+    tot_f, tot_s, desc = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        f, s, desc = oracle_sample(w, per_step)
+        tot_f += f
+        tot_s += s
+    value = tot_f / tot_s / 1e12
+    B, H, N, d = w.shape
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot_s * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "kind": "oracle",
+                             "cores": oracle.num_threads(), "sample": desc},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--shape", default=None,
+                    help="B,H,N,d,causal: a smaller same-recipe case (profiling only)")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0,
+                    help="CPU time budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, _, _ = dist_env()
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world} (launch N>1 with torchrun)")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,103 @@
+"""Torch-facing helpers over the C ABI.
+
+PyTorch only supplies device memory and the current stream; the tensors'
+data pointers go straight to ``fa_fwd`` / ``fa_bwd``.  Inputs must be CUDA
+bf16 tensors, contiguous, shaped [B, H, N, d].
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+
+
+def _stream_handle(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check_inputs(*ts: torch.Tensor) -> Tuple[int, int, int, int]:
+    ref = ts[0]
+    if ref.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    for t in ts:
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA bf16 tensors")
+        if t.shape != ref.shape or t.device != ref.device:
+            raise ValueError("inputs must share shape and device")
+    B, H, N, d = ref.shape
+    return B, H, N, d
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool,
+        tau: Optional[float] = None, out: Optional[torch.Tensor] = None,
+        lse: Optional[torch.Tensor] = None, o_fp32: bool = False):
+    """Forward pass.  Returns (O, LSE): O bf16 (fp32 with ``o_fp32``) and LSE
+    fp32 [B, H, N]."""
+    B, H, N, d = _check_inputs(q, k, v)
+    tau = 1.0 / math.sqrt(d) if tau is None else float(tau)
+    o_dtype = torch.float32 if o_fp32 else torch.bfloat16
+    if out is None:
+        out = torch.empty(q.shape, dtype=o_dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    fn = _lib.fa_fwd_o32 if o_fp32 else _lib.fa_fwd
+    code = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+              B, H, N, d, tau, int(bool(causal)), _stream_handle(q.device))
+    _lib.check(code, "fa_fwd_o32" if o_fp32 else "fa_fwd")
+    return out, lse
+
+
+def workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return _lib.fa_bwd_workspace_size(B, H, N, d)
+
+
+def bwd(q, k, v, o, do, lse, causal: bool, tau: Optional[float] = None,
+        dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
+        dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """Backward pass.  Returns (dQ, dK, dV), bf16.  ``workspace`` (a byte
+    tensor of at least ``workspace_bytes`` bytes) is allocated with torch when
+    not given, so the library itself allocates nothing."""
+    B, H, N, d = _check_inputs(q, k, v, o, do)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or lse.shape != (B, H, N):
+        raise ValueError("lse must be contiguous fp32 [B, H, N]")
+    tau = 1.0 / math.sqrt(d) if tau is None else float(tau)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    code = _lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                       workspace.data_ptr(), workspace.numel(), B, H, N, d, tau,
+                       int(bool(causal)), _stream_handle(q.device))
+    _lib.check(code, "fa_bwd")
+    return dq, dk, dv
+
+
+def last_device_error(device: Optional[torch.device] = None) -> int:
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    return _lib.fa_last_device_error(_stream_handle(device))
+
+
+class _Attention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, causal, tau):
+        o, lse = fwd(q, k, v, causal, tau)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.causal, ctx.tau = causal, tau
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = bwd(q, k, v, o, do.contiguous(), lse, ctx.causal, ctx.tau)
+        return dq, dk, dv, None, None
+
+
+def attention(q, k, v, causal: bool = False, tau: Optional[float] = None) -> torch.Tensor:
+    """O = softmax(tau Q K^T [causal]) V with autograd support."""
+    return _Attention.apply(q, k, v, causal, tau)

@@ -1,0 +1,572 @@
+// Backward kernels of exact IO-aware attention for sm_103a.
+//
+// Method (tonho.wtf "flash attention" entry, section "como funciona",
+// backward paragraph; "FlashAttention: O Que E e Como Acelera LLMs na
+// Pratica", pillar 2): the backward keeps only O and the per-row statistics
+// (packed as LSE), rebuilds S and P on chip, and replaces the softmax
+// Jacobian's row sum by D_i = dO_i . O_i.  With dP = dO V^T and
+// dS = P o (dP - D):  dV = P^T dO,  dK = tau dS^T Q,  dQ = tau dS K.
+//
+// Three kernels:
+//   bwd_pre   D_i = sum_k dO_ik O_ik (fp32) and a zeroed fp32 dQ accumulator.
+//   bwd_main  one CTA per (128-key tile, batch*head); it walks the query tiles
+//             that can see its keys (all of them, or those at or below the
+//             diagonal when causal):
+//               S^T  = K Q_i^T            tcgen05, both operands in smem
+//               dP^T = V dO_i^T           tcgen05
+//               P^T  = exp2(c S^T - log2e LSE_i)   warps 0-3, written back to
+//                                         tensor memory as bf16 over S^T
+//               dV  += P^T dO_i           tcgen05, A read from tensor memory
+//               dS^T = P^T o (dP^T - D_i) warps 0-3, to tensor memory (over
+//                                         dP^T) and to smem
+//               dK  += dS^T Q_i           tcgen05, A from tensor memory
+//               dQ_i = dS K               tcgen05, A = dS^T from smem
+//             warps 4-7 read dQ_i out of tensor memory and add it into the
+//             fp32 accumulator with TMA bulk reductions (no per-element
+//             atomics); at the end they write dK (scaled by tau) and dV.
+//             warp 8 loads (TMA), warp 9 issues the MMAs.
+//   bwd_post  dQ = bf16(tau * accumulator).
+// Tensor memory (512 columns): dV and dK accumulators (d each), S^T (128),
+// dP^T (128); for d = 128 the dQ tile reuses the S^T columns once P^T has
+// been consumed, so the next S^T waits until dQ has been read out.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBQ = 128;  // query rows per step
+constexpr int kBK = 128;  // keys per CTA
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kLog2e = 1.44269504088896341f;
+
+template <int D>
+struct BwdLayout {
+    static constexpr int kTile = kBK * D * 2;  // one bf16 [128 x D] tile
+    static constexpr int kBox = 128 * 128;     // [128 rows x 64 bf16] or [128 x 32 fp32]
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kK = 0;
+    static constexpr int kV = kTile;
+    static constexpr int kStage0 = 2 * kTile;    // stage s: Q at +0, dO at +kTile
+    static constexpr int kStageBytes = 2 * kTile;
+    static constexpr int kDS = kStage0 + 2 * kStageBytes;  // dS^T [128 keys x 128 queries] bf16
+    static constexpr int kDSBytes = 128 * 128 * 2;
+    static constexpr int kVec = kDS + kDSBytes;  // lse2[2][128], dvec[2][128]
+    static constexpr int kBars = kVec + 4 * 128 * 4;
+    static constexpr int kBytes = kBars + 256;
+    // tensor-memory columns
+    static constexpr uint32_t kTmDV = 0, kTmDK = D, kTmS = 2 * D, kTmDP = 2 * D + 128;
+    static constexpr bool kDQAliasS = (D == 128);
+    static constexpr uint32_t kTmDQ = kDQAliasS ? kTmS : 2 * D + 256;
+};
+
+struct BwdBarriers {
+    uint64_t kv_full;
+    uint64_t qdo_full[2];
+    uint64_t qdo_empty[2];
+    uint64_t s_full;
+    uint64_t dp_full;
+    uint64_t p_ready;
+    uint64_t ds_ready;
+    uint64_t dq_full;
+    uint64_t dq_drained;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+struct BwdParams {
+    const float* LSE;
+    const float* Dvec;
+    int N;
+    int n_kv;
+    float scale_log2;  // tau * log2(e)
+    float tau;
+    unsigned int* err;
+    unsigned long long wait_limit_ns;
+};
+
+enum : uint32_t {
+    kSiteProd = 21, kSiteMmaKV = 22, kSiteMmaQ = 23, kSiteMmaP = 24, kSiteMmaDS = 25,
+    kSiteMmaDrain = 26, kSiteDsS = 27, kSiteDsQ = 28, kSiteDsDP = 29, kSiteDsDQ = 30,
+    kSiteDrain = 31
+};
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+// D = A B^T, both K-major tiles of 128 rows x Dk (two 64-column boxes when Dk = 128).
+template <int Dk>
+__device__ __forceinline__ void mma_rows_rows(uint32_t tmem_d, uint32_t a, uint32_t b) {
+    constexpr uint32_t id = idesc_bf16(128, 128, false, false);
+#pragma unroll
+    for (int k = 0; k < Dk / 16; ++k) {
+        const uint32_t off = (k / 4) * (128 * 128) + (k % 4) * 32;
+        mma_ss(tmem_d, sw128_desc(a + off, 16, 1024), sw128_desc(b + off, 16, 1024), id, k > 0);
+    }
+}
+
+// D (+)= A_tmem[128 x 128] B, B an MN-major smem tile [128 rows(K) x N] (N = Dn).
+template <int Dn>
+__device__ __forceinline__ void mma_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint32_t b,
+                                           bool accumulate) {
+    constexpr uint32_t id = idesc_bf16(128, Dn, false, true);
+#pragma unroll
+    for (int k = 0; k < 128 / 16; ++k)
+        mma_ts(tmem_d, tmem_a + k * 8, sw128_desc(b + k * 2048, 128 * 128, 1024), id,
+               accumulate || k > 0);
+}
+
+// D = A B with A MN-major [128(K) x 128(M)] and B MN-major [128(K) x Dn].
+template <int Dn>
+__device__ __forceinline__ void mma_mn_mn(uint32_t tmem_d, uint32_t a, uint32_t b) {
+    constexpr uint32_t id = idesc_bf16(128, Dn, true, true);
+#pragma unroll
+    for (int k = 0; k < 128 / 16; ++k)
+        mma_ss(tmem_d, sw128_desc(a + k * 2048, 128 * 128, 1024),
+               sw128_desc(b + k * 2048, 128 * 128, 1024), id, k > 0);
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                   const __grid_constant__ CUtensorMap tmdQacc,
+                   const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                   const BwdParams p) {
+    using L = BwdLayout<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sbase = smem_addr(smem);
+    BwdBarriers& sh = *reinterpret_cast<BwdBarriers*>(smem + L::kBars);
+    float* lse2_s = reinterpret_cast<float*>(smem + L::kVec);        // [2][128]
+    float* dvec_s = reinterpret_cast<float*>(smem + L::kVec + 1024);  // [2][128]
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int kv_tile = blockIdx.y;  // tile 0 has the most query tiles when causal
+    const int N = p.N;
+    const int kv_start = kv_tile * kBK;
+    const int n_q = (N + kBQ - 1) / kBQ;
+    const int first = CAUSAL ? kv_tile : 0;
+    const int n_steps = n_q - first;
+
+    if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
+        if (threadIdx.x == 0) atomicCAS(p.err, 0u, 1u | (0xAAu << 8));
+        return;
+    }
+
+    const uint32_t bar_kv = smem_addr(&sh.kv_full);
+    const uint32_t bar_qf = smem_addr(&sh.qdo_full[0]);
+    const uint32_t bar_qe = smem_addr(&sh.qdo_empty[0]);
+    const uint32_t bar_s = smem_addr(&sh.s_full);
+    const uint32_t bar_dp = smem_addr(&sh.dp_full);
+    const uint32_t bar_p = smem_addr(&sh.p_ready);
+    const uint32_t bar_ds = smem_addr(&sh.ds_ready);
+    const uint32_t bar_dq = smem_addr(&sh.dq_full);
+    const uint32_t bar_dr = smem_addr(&sh.dq_drained);
+
+    if (threadIdx.x == 0) {
+        sh.abort_flag = 0;
+        mbar_init(bar_kv, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar_qf + 8 * s, 32);
+            mbar_init(bar_qe + 8 * s, 2);
+        }
+        mbar_init(bar_s, 1);
+        mbar_init(bar_dp, 1);
+        mbar_init(bar_p, 128);
+        mbar_init(bar_ds, 128);
+        mbar_init(bar_dq, 1);
+        mbar_init(bar_dr, 128);
+        mbar_init_fence();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(&sh.tmem_base), 512);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_map(&tmQ);
+        tma_prefetch_map(&tmK);
+        tma_prefetch_map(&tmV);
+        tma_prefetch_map(&tmdO);
+        tma_prefetch_map(&tmdQacc);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    const Watchdog wd{p.err, &sh.abort_flag, p.wait_limit_ns};
+    constexpr uint32_t FULL = 0xffffffffu;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------- producer --
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar_kv, 2 * L::kTile);
+            for (int b = 0; b < L::kBoxes; ++b) {
+                tma_load_3d(sbase + L::kK + b * L::kBox, &tmK, bar_kv, b * 64, kv_start, bh);
+                tma_load_3d(sbase + L::kV + b * L::kBox, &tmV, bar_kv, b * 64, kv_start, bh);
+            }
+        }
+        for (int s = 0; s < n_steps; ++s) {
+            const int st = s & 1;
+            if (s >= 2 && !mbar_wait(bar_qe + 8 * st, ((s >> 1) - 1) & 1, wd, kSiteProd)) break;
+            const int q_start = (first + s) * kBQ;
+            const int64_t row0 = static_cast<int64_t>(bh) * N;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c = lane * 4 + e;
+                const int q = q_start + c;
+                lse2_s[st * 128 + c] = q < N ? p.LSE[row0 + q] * kLog2e : INFINITY;
+                dvec_s[st * 128 + c] = q < N ? p.Dvec[row0 + q] : 0.f;
+            }
+            const uint32_t stage = sbase + L::kStage0 + st * L::kStageBytes;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar_qf + 8 * st, 2 * L::kTile);
+                for (int b = 0; b < L::kBoxes; ++b) {
+                    tma_load_3d(stage + b * L::kBox, &tmQ, bar_qf + 8 * st, b * 64, q_start, bh);
+                    tma_load_3d(stage + L::kTile + b * L::kBox, &tmdO, bar_qf + 8 * st, b * 64,
+                                q_start, bh);
+                }
+            } else {
+                mbar_arrive(bar_qf + 8 * st);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA --
+        if (lane == 0) {
+            const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sDS = sbase + L::kDS;
+            bool ok = mbar_wait(bar_kv, 0, wd, kSiteMmaKV) && mbar_wait(bar_qf, 0, wd, kSiteMmaQ);
+            if (ok) {
+                tc_fence_after();
+                const uint32_t stage = sbase + L::kStage0;
+                mma_rows_rows<D>(tmem + L::kTmS, sK, stage);              // S^T
+                mma_commit(bar_s);
+                mma_rows_rows<D>(tmem + L::kTmDP, sV, stage + L::kTile);  // dP^T
+                mma_commit(bar_dp);
+            }
+            for (int s = 0; ok && s < n_steps; ++s) {
+                const int st = s & 1;
+                const uint32_t stage = sbase + L::kStage0 + st * L::kStageBytes;
+                if (!mbar_wait(bar_p, s & 1, wd, kSiteMmaP)) { ok = false; break; }
+                tc_fence_after();
+                mma_tmem_a<D>(tmem + L::kTmDV, tmem + L::kTmS, stage + L::kTile, s > 0);  // dV
+                if (!mbar_wait(bar_ds, s & 1, wd, kSiteMmaDS)) { ok = false; break; }
+                tc_fence_after();
+                mma_tmem_a<D>(tmem + L::kTmDK, tmem + L::kTmDP, stage, s > 0);            // dK
+                if (!L::kDQAliasS && s > 0) {
+                    if (!mbar_wait(bar_dr, (s - 1) & 1, wd, kSiteMmaDrain)) { ok = false; break; }
+                    tc_fence_after();
+                }
+                mma_mn_mn<D>(tmem + L::kTmDQ, sDS, sK);                                   // dQ
+                mma_commit(bar_dq);
+                mma_commit(bar_qe + 8 * st);
+                if (s + 1 < n_steps) {
+                    const int st1 = (s + 1) & 1;
+                    const uint32_t stage1 = sbase + L::kStage0 + st1 * L::kStageBytes;
+                    if (!mbar_wait(bar_qf + 8 * st1, ((s + 1) >> 1) & 1, wd, kSiteMmaQ)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    mma_rows_rows<D>(tmem + L::kTmDP, sV, stage1 + L::kTile);  // dP^T next
+                    mma_commit(bar_dp);
+                    if (L::kDQAliasS) {
+                        if (!mbar_wait(bar_dr, s & 1, wd, kSiteMmaDrain)) { ok = false; break; }
+                        tc_fence_after();
+                    }
+                    mma_rows_rows<D>(tmem + L::kTmS, sK, stage1);              // S^T next
+                    mma_commit(bar_s);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------- P^T and dS^T (keys) --
+        const int k = threadIdx.x;  // key row within the tile = tensor-memory lane
+        const int kg = kv_start + k;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tS = tmem + lane_off + L::kTmS;
+        const uint32_t tDP = tmem + lane_off + L::kTmDP;
+        const float sl2 = p.scale_log2;
+        uint8_t* ds_row = smem + L::kDS + k * 128;
+        for (int s = 0; s < n_steps; ++s) {
+            const int st = s & 1;
+            const int q_start = (first + s) * kBQ;
+            bool got = mbar_wait(bar_s, s & 1, wd, kSiteDsS) &&
+                       mbar_wait(bar_qf + 8 * st, (s >> 1) & 1, wd, kSiteDsQ);
+            if (!__all_sync(FULL, got)) break;
+            tc_fence_after();
+            const float* l2 = lse2_s + st * 128;
+            const bool diag = CAUSAL && (q_start == kv_start);
+            // P^T = exp2(c S^T - log2e LSE), bf16, over the S^T columns
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                uint32_t sv[32];
+                tmem_ld32(tS + h * 32, sv);
+                tmem_ld_wait(sv);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int c = h * 32 + 2 * i;
+                    float p0 = ex2(fmaf(u2f(sv[2 * i]), sl2, -l2[c]));
+                    float p1 = ex2(fmaf(u2f(sv[2 * i + 1]), sl2, -l2[c + 1]));
+                    if (diag) {
+                        if (kg > q_start + c) p0 = 0.f;
+                        if (kg > q_start + c + 1) p1 = 0.f;
+                    }
+                    if (kg >= N) p0 = p1 = 0.f;  // key row past a ragged end
+                    pk[i] = pack_bf16(p0, p1);
+                }
+                tmem_st16(tS + h * 16, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar_p);
+
+            got = mbar_wait(bar_dp, s & 1, wd, kSiteDsDP);
+            if (got && s > 0) got = mbar_wait(bar_dq, (s - 1) & 1, wd, kSiteDsDQ);  // dS smem free
+            if (!__all_sync(FULL, got)) break;
+            tc_fence_after();
+            const float* dv = dvec_s + st * 128;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                uint32_t dp[32], pk[16];
+                tmem_ld32(tDP + h * 32, dp);
+                tmem_ld16(tS + h * 16, pk);
+                tmem_ld_wait(dp);
+                tmem_ld_wait(pk);
+                uint32_t ds[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int c = h * 32 + 2 * i;
+                    const float p0 = u2f(pk[i] << 16), p1 = u2f(pk[i] & 0xffff0000u);
+                    ds[i] = pack_bf16(p0 * (u2f(dp[2 * i]) - dv[c]),
+                                      p1 * (u2f(dp[2 * i + 1]) - dv[c + 1]));
+                }
+                tmem_st16(tDP + h * 16, ds);
+                // smem copy for the dQ MMA: row k, queries 32h..32h+31 (4 x 16 bytes)
+                uint8_t* sub = ds_row + (h >> 1) * (128 * 128);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int chunk = (h & 1) * 4 + q4;
+                    *reinterpret_cast<uint4*>(sub + ((chunk ^ (k & 7)) << 4)) =
+                        make_uint4(ds[4 * q4], ds[4 * q4 + 1], ds[4 * q4 + 2], ds[4 * q4 + 3]);
+                }
+            }
+            fence_async_shared();
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bar_ds);
+        }
+    } else {
+        // ------------------------------- dQ drain and dK/dV epilogue (4-7) --
+        const int r = threadIdx.x - 128;  // query row (dQ) / key row (dK, dV)
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tDQ = tmem + lane_off + L::kTmDQ;
+        bool ok = true;
+        for (int s = 0; s < n_steps; ++s) {
+            const int st = s & 1;
+            const int q_start = (first + s) * kBQ;
+            // the exit decision must be the same for all 128 threads: they share
+            // the named barrier below
+            if (named_bar_or(3, 128, !mbar_wait(bar_dq, s & 1, wd, kSiteDrain))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t acc[D / 32][32];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(tDQ + c * 32, acc[c]);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_ld_wait(acc[c]);
+            tc_fence_before();
+            mbar_arrive(bar_dr);
+            // stage Q_i + dO_i (free now) as D/32 fp32 boxes of [128 rows x 32 cols]
+            uint8_t* stage = smem + L::kStage0 + st * L::kStageBytes;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<uint4*>(stage + c * L::kBox + r * 128 + ((j ^ (r & 7)) << 4)) =
+                        make_uint4(acc[c][4 * j], acc[c][4 * j + 1], acc[c][4 * j + 2],
+                                   acc[c][4 * j + 3]);
+            }
+            fence_async_shared();
+            named_bar_sync(2, 128);
+            if (r == 0) {
+                const uint32_t src = sbase + L::kStage0 + st * L::kStageBytes;
+                for (int c = 0; c < D / 32; ++c)
+                    tma_reduce_add_3d(&tmdQacc, src + c * L::kBox, c * 32, q_start, bh);
+                bulk_commit();
+                bulk_wait_read<0>();
+                mbar_arrive(bar_qe + 8 * st);
+            }
+        }
+        // dK = tau * dK_acc and dV, staged over the K and V tiles (no MMA reads them now)
+        if (ok) {
+            tc_fence_after();
+            const uint32_t tDV = tmem + lane_off + L::kTmDV, tDK = tmem + lane_off + L::kTmDK;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                uint8_t* dst = smem + (which ? L::kK : L::kV);
+                const float scale = which ? p.tau : 1.f;
+                const uint32_t src = which ? tDK : tDV;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(src + c0, o);
+                    tmem_ld_wait(o);
+                    const int box = c0 / 64;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int chunk = (c0 % 64) / 8 + q;
+                        uint4 v;
+                        v.x = pack_bf16(u2f(o[8 * q + 0]) * scale, u2f(o[8 * q + 1]) * scale);
+                        v.y = pack_bf16(u2f(o[8 * q + 2]) * scale, u2f(o[8 * q + 3]) * scale);
+                        v.z = pack_bf16(u2f(o[8 * q + 4]) * scale, u2f(o[8 * q + 5]) * scale);
+                        v.w = pack_bf16(u2f(o[8 * q + 6]) * scale, u2f(o[8 * q + 7]) * scale);
+                        *reinterpret_cast<uint4*>(dst + box * L::kBox + r * 128 +
+                                                  ((chunk ^ (r & 7)) << 4)) = v;
+                    }
+                }
+            }
+            fence_async_shared();
+        }
+        named_bar_sync(2, 128);
+        if (r == 0 && ok) {
+            for (int b = 0; b < L::kBoxes; ++b) {
+                tma_store_3d(&tmdV, sbase + L::kV + b * L::kBox, b * 64, kv_start, bh);
+                tma_store_3d(&tmdK, sbase + L::kK + b * L::kBox, b * 64, kv_start, bh);
+            }
+            bulk_commit();
+            bulk_wait_read<0>();
+        }
+    }
+
+    // ------------------------------------------------------------ teardown --
+    if (sh.abort_flag) drain_after_abort();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// D_i = dO_i . O_i in fp32 and a zeroed dQ accumulator row; D/8 threads per row,
+// each handling 8 bf16 of both inputs (16-byte loads).
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ O,
+                                                         const __nv_bfloat16* __restrict__ dO,
+                                                         float* __restrict__ Dvec,
+                                                         float* __restrict__ dQacc, int64_t rows) {
+    constexpr int TPR = D / 8;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t row = tid / TPR;
+    const int sub = static_cast<int>(tid % TPR);
+    float acc = 0.f;
+    if (row < rows) {
+        const uint4 a = *reinterpret_cast<const uint4*>(O + row * D + sub * 8);
+        const uint4 b = *reinterpret_cast<const uint4*>(dO + row * D + sub * 8);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc = fmaf(u2f(aw[i] << 16), u2f(bw[i] << 16), acc);
+            acc = fmaf(u2f(aw[i] & 0xffff0000u), u2f(bw[i] & 0xffff0000u), acc);
+        }
+        float4* z = reinterpret_cast<float4*>(dQacc + row * D + sub * 8);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && sub == 0) Dvec[row] = acc;
+}
+
+// dQ = bf16(tau * acc), 8 elements per thread, grid-stride.
+__global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restrict__ acc,
+                                                          __nv_bfloat16* __restrict__ dQ,
+                                                          float tau, int64_t n8) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+        const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+        uint4 o;
+        o.x = pack_bf16(a.x * tau, a.y * tau);
+        o.y = pack_bf16(a.z * tau, a.w * tau);
+        o.z = pack_bf16(b.x * tau, b.y * tau);
+        o.w = pack_bf16(b.z * tau, b.w * tau);
+        reinterpret_cast<uint4*>(dQ)[i] = o;
+    }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+    using L = BwdLayout<D>;
+    const int64_t rows = static_cast<int64_t>(a.BH) * a.N;
+    // 1. D and a zeroed accumulator
+    {
+        constexpr int TPR = D / 8;
+        const int64_t threads = rows * TPR;
+        const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+        fa_bwd_pre_kernel<D><<<blocks, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.D,
+            a.dQacc, rows);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // 2. main kernel
+    {
+        CUtensorMap tq, tk, tv, tdo, tacc, tdk, tdv;
+        const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        if (!make_tile_map(&tq, a.Q, BF, 2, D, a.N, a.BH, 64, kBQ) ||
+            !make_tile_map(&tk, a.K, BF, 2, D, a.N, a.BH, 64, kBK) ||
+            !make_tile_map(&tv, a.V, BF, 2, D, a.N, a.BH, 64, kBK) ||
+            !make_tile_map(&tdo, a.dO, BF, 2, D, a.N, a.BH, 64, kBQ) ||
+            !make_tile_map(&tacc, a.dQacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, a.N, a.BH, 32, kBQ) ||
+            !make_tile_map(&tdk, a.dK, BF, 2, D, a.N, a.BH, 64, kBK) ||
+            !make_tile_map(&tdv, a.dV, BF, 2, D, a.N, a.BH, 64, kBK))
+            return cudaErrorInvalidValue;
+        auto kern = fa_bwd_main_kernel<D, CAUSAL>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+        if (e != cudaSuccess) return e;
+        BwdParams p;
+        p.LSE = a.LSE;
+        p.Dvec = a.D;
+        p.N = a.N;
+        p.n_kv = (a.N + kBK - 1) / kBK;
+        p.scale_log2 = a.tau * kLog2e;
+        p.tau = a.tau;
+        p.err = a.err;
+        p.wait_limit_ns = a.wait_limit_ns;
+        dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(p.n_kv));
+        if (a.ev_start) cudaEventRecord(a.ev_start, stream);
+        kern<<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tacc, tdk, tdv, p);
+        e = cudaGetLastError();
+        if (e == cudaSuccess && a.ev_stop) e = cudaEventRecord(a.ev_stop, stream);
+        if (e != cudaSuccess) return e;
+    }
+    // 3. dQ = tau * accumulator
+    {
+        const int64_t n8 = rows * D / 8;
+        int64_t blocks = (n8 + 255) / 256;
+        if (blocks > 152 * 64) blocks = 152 * 64;
+        fa_bwd_post_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            a.dQacc, static_cast<__nv_bfloat16*>(a.dQ), a.tau, n8);
+        return cudaGetLastError();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+    if (a.d == 64) return a.causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
+    return a.causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
+}
+
+}  // namespace fa

@@ -1,0 +1,472 @@
+// Forward kernel of exact IO-aware attention for sm_103a.
+//
+// Method (tonho.wtf "flash attention" entry, section "como funciona";
+// "Atencao eficiente - FlashAttention, sparse e hibrida", "Insight 1 -
+// Tiling" and "Insight 2 - Online softmax"): the scores of one query tile
+// against one key block live only on chip; each row carries its running max m
+// and sum l, and merging a new block rescales what was accumulated.  The N x N
+// matrix never reaches device memory; only O and LSE = m + ln l are written.
+//
+// GB300 design (differs from the pages' A100 loop order, which walks key
+// blocks outside and reloads O/m/l per query block):
+//   - one CTA owns two 128-row query tiles of one (batch, head) and walks the
+//     key blocks inside, so O, m and l never leave the chip;
+//   - warp 8 streams K_j and V_j with TMA (128-byte swizzle) through a ring
+//     of shared-memory slots guarded by full/empty mbarriers;
+//   - warp 9 issues tcgen05.mma: S_t = Q_t K_j^T into tensor memory (fp32),
+//     then O_t += P_t V_j with P_t read from tensor memory (bf16, written
+//     over S_t's columns by the softmax warps);
+//   - warps 0-3 / 4-7 run the online softmax of tile 0 / tile 1 (one thread
+//     per row = one tensor-memory lane), so one tile's softmax overlaps the
+//     other tile's MMAs;
+//   - the exponent is taken with ex2 on tau*log2(e)-scaled scores; O is
+//     rescaled only when a row's max grows by more than 2^8 (the stale max
+//     is used for both O and l, so the final O / l is unchanged);
+//   - causal: key blocks wholly above the diagonal are never loaded; the
+//     diagonal block is masked element-wise.  Keys >= N in a ragged last
+//     block are masked the same way.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128;  // query rows per tile
+constexpr int kBN = 128;  // keys per block
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kLog2e = 1.44269504088896341f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
+
+template <int D>
+struct FwdLayout {
+    static constexpr int kTileBytes = kBM * D * 2;  // one 128-row bf16 tile
+    static constexpr int kBoxBytes = 128 * 128;     // one [128 rows x 64 cols] bf16 TMA box
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kStages = (D == 64) ? 8 : 4;
+    static constexpr int kQ0 = 0;
+    static constexpr int kQ1 = kTileBytes;
+    static constexpr int kRing = 2 * kTileBytes;
+    static constexpr int kBytes = kRing + kStages * kTileBytes;
+    static constexpr int kDynSmem = kBytes + 1024;  // + alignment slack
+    static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128;
+    static constexpr uint32_t kTmemO0 = 256, kTmemO1 = 256 + D;
+};
+
+struct FwdParams {
+    float* LSE;
+    float* O32;
+    int N;
+    int n_pairs;
+    float scale_log2;  // tau * log2(e)
+    unsigned int* err;
+    unsigned long long wait_limit_ns;
+};
+
+struct FwdShared {
+    uint64_t q_full;
+    uint64_t kv_full[8];
+    uint64_t kv_empty[8];
+    uint64_t s_full[2];
+    uint64_t p_ready[2];
+    uint64_t o_done[2];
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// Wait-site ids recorded in the error word.
+enum : uint32_t {
+    kSiteProdEmpty = 1, kSiteMmaQ = 2, kSiteMmaKV = 3, kSiteMmaP = 4,
+    kSiteSoftS = 5, kSiteSoftO = 6, kSiteEpi = 7
+};
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32_t k_smem) {
+    constexpr uint32_t id = idesc_bf16(128, 128, false, false);
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k / 4) * (128 * 128) + (k % 4) * 32;
+        mma_ss(tmem_d, sw128_desc(q_smem + off, 16, 1024), sw128_desc(k_smem + off, 16, 1024), id,
+               k > 0);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_smem,
+                                         bool accumulate) {
+    constexpr uint32_t id = idesc_bf16(128, D, false, true);
+#pragma unroll
+    for (int k = 0; k < kBN / 16; ++k) {
+        mma_ts(tmem_o, tmem_p + k * 8, sw128_desc(v_smem + k * 2048, 128 * 128, 1024), id,
+               accumulate || k > 0);
+    }
+}
+
+template <int D, bool CAUSAL, bool O32>
+__global__ void __launch_bounds__(kThreads, 1)
+fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+              const FwdParams p) {
+    using L = FwdLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ FwdShared sh;
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+    uint8_t* smem = smem_raw + pad;
+    const uint32_t sbase = raw + pad;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.y);  // heaviest pairs first
+    const int N = p.N;
+    const int n_kv = (N + kBN - 1) / kBN;
+    const int q_start0 = pair * 2 * kBM;
+    const int q_start1 = q_start0 + kBM;
+    int n_blk0 = CAUSAL ? min(n_kv, q_start0 / kBN + 1) : n_kv;
+    int n_blk1 = q_start1 < N ? (CAUSAL ? min(n_kv, q_start1 / kBN + 1) : n_kv) : 0;
+    const int nb = max(n_blk0, n_blk1);
+
+    const uint32_t bar_q = smem_addr(&sh.q_full);
+    const uint32_t bar_kv_full = smem_addr(&sh.kv_full[0]);
+    const uint32_t bar_kv_empty = smem_addr(&sh.kv_empty[0]);
+    const uint32_t bar_s = smem_addr(&sh.s_full[0]);
+    const uint32_t bar_p = smem_addr(&sh.p_ready[0]);
+    const uint32_t bar_o = smem_addr(&sh.o_done[0]);
+
+    if (threadIdx.x == 0) {
+        sh.abort_flag = 0;
+        mbar_init(bar_q, 1);
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(bar_kv_full + 8 * s, 1);
+            mbar_init(bar_kv_empty + 8 * s, 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar_s + 8 * t, 1);
+            mbar_init(bar_p + 8 * t, 128);
+            mbar_init(bar_o + 8 * t, 1);
+        }
+        mbar_init_fence();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(&sh.tmem_base), 512);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_map(&tmQ);
+        tma_prefetch_map(&tmK);
+        tma_prefetch_map(&tmV);
+        if (!O32) tma_prefetch_map(&tmO);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    const Watchdog wd{p.err, &sh.abort_flag, p.wait_limit_ns};
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------- producer --
+        if (lane == 0) {
+            uint32_t qbytes = L::kTileBytes * ((n_blk0 > 0) + (n_blk1 > 0));
+            mbar_arrive_expect_tx(bar_q, qbytes);
+            for (int b = 0; b < L::kBoxes; ++b) {
+                tma_load_3d(sbase + L::kQ0 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start0, bh);
+                if (n_blk1 > 0)
+                    tma_load_3d(sbase + L::kQ1 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start1, bh);
+            }
+            for (int ld = 0; ld < 2 * nb; ++ld) {
+                const int slot = ld % L::kStages;
+                if (ld >= L::kStages &&
+                    !mbar_wait(bar_kv_empty + 8 * slot, ((ld / L::kStages) - 1) & 1, wd, kSiteProdEmpty))
+                    break;
+                const CUtensorMap* map = (ld & 1) ? &tmV : &tmK;
+                const uint32_t dst = sbase + L::kRing + slot * L::kTileBytes;
+                mbar_arrive_expect_tx(bar_kv_full + 8 * slot, L::kTileBytes);
+                for (int b = 0; b < L::kBoxes; ++b)
+                    tma_load_3d(dst + b * L::kBoxBytes, map, bar_kv_full + 8 * slot, b * 64,
+                                (ld >> 1) * kBN, bh);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA --
+        if (lane == 0) {
+            const uint32_t tS[2] = {tmem + L::kTmemS0, tmem + L::kTmemS1};
+            const uint32_t tO[2] = {tmem + L::kTmemO0, tmem + L::kTmemO1};
+            const uint32_t sQ[2] = {sbase + L::kQ0, sbase + L::kQ1};
+            const int nblk[2] = {n_blk0, n_blk1};
+            bool ok = mbar_wait(bar_q, 0, wd, kSiteMmaQ) &&
+                      mbar_wait(bar_kv_full, 0, wd, kSiteMmaKV);
+            if (ok) {
+                tc_fence_after();
+                const uint32_t k0 = sbase + L::kRing;
+                for (int t = 0; t < 2; ++t) {
+                    if (nblk[t] > 0) {
+                        issue_s<D>(tS[t], sQ[t], k0);
+                        mma_commit(bar_s + 8 * t);
+                    }
+                }
+                mma_commit(bar_kv_empty);
+            }
+            for (int j = 0; ok && j < nb; ++j) {
+                const int lv = 2 * j + 1, lk = 2 * j + 2;
+                const int sv = lv % L::kStages, sk = lk % L::kStages;
+                if (!mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1, wd, kSiteMmaKV)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                bool k_ready = false;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= nblk[t]) continue;
+                    if (!mbar_wait(bar_p + 8 * t, j & 1, wd, kSiteMmaP)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv<D>(tO[t], tS[t], sbase + L::kRing + sv * L::kTileBytes, j > 0);
+                    mma_commit(bar_o + 8 * t);
+                    if (j + 1 < nblk[t]) {
+                        if (!k_ready) {
+                            if (!mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1, wd,
+                                           kSiteMmaKV)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            k_ready = true;
+                        }
+                        issue_s<D>(tS[t], sQ[t], sbase + L::kRing + sk * L::kTileBytes);
+                        mma_commit(bar_s + 8 * t);
+                    }
+                }
+                if (!ok) break;
+                mma_commit(bar_kv_empty + 8 * sv);
+                if (k_ready) mma_commit(bar_kv_empty + 8 * sk);
+            }
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------------- softmax --
+        const int t = warp >> 2;
+        const int r = threadIdx.x & 127;
+        const int q_start = t ? q_start1 : q_start0;
+        const int nbt = t ? n_blk1 : n_blk0;
+        const int row = q_start + r;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_off + (t ? L::kTmemS1 : L::kTmemS0);
+        const uint32_t tO = tmem + lane_off + (t ? L::kTmemO1 : L::kTmemO0);
+        const uint32_t my_s = bar_s + 8 * t, my_p = bar_p + 8 * t, my_o = bar_o + 8 * t;
+        const float sl2 = p.scale_log2;
+        float m_used = -INFINITY;
+        float l = 0.f, l_mma = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nbt; ++j) {
+            // wait results are made warp-uniform: tcgen05.ld/st are warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait(my_s, j & 1, wd, kSiteSoftS))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t s[4][32];
+            tmem_ld32(tS + 0, s[0]);
+            tmem_ld32(tS + 32, s[1]);
+            tmem_ld32(tS + 64, s[2]);
+            tmem_ld32(tS + 96, s[3]);
+            tmem_ld_wait(s[0]);
+            tmem_ld_wait(s[1]);
+            tmem_ld_wait(s[2]);
+            tmem_ld_wait(s[3]);
+
+            const int kbase = j * kBN;
+            const bool need_mask = (CAUSAL && kbase + kBN - 1 > q_start) || (kbase + kBN > N);
+            if (need_mask) {
+                const int last = CAUSAL ? min(row, N - 1) : N - 1;  // last visible key
+#pragma unroll
+                for (int c = 0; c < 128; ++c)
+                    if (kbase + c > last) s[c >> 5][c & 31] = f2u(-INFINITY);
+            }
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                mx0 = fmaxf(mx0, u2f(s[0][c]));
+                mx1 = fmaxf(mx1, u2f(s[1][c]));
+                mx2 = fmaxf(mx2, u2f(s[2][c]));
+                mx3 = fmaxf(mx3, u2f(s[3][c]));
+            }
+            const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+            const bool grow = m_cand > m_used + kRescaleThreshold;
+            float alpha = 1.f;
+            if (grow) {
+                alpha = ex2(m_used - m_cand);  // 0 on the first block (m_used = -inf)
+                m_used = m_cand;
+            }
+            l *= alpha;
+            l_mma *= alpha;
+            const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+            // Two row sums: l_mma over the bf16 P values the P.V MMA consumes (it
+            // normalises O, so the weights actually applied sum to one) and l over
+            // the fp32 values (it gives LSE).
+            float ls0 = 0.f, ls1 = 0.f, lr0 = 0.f, lr1 = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int c = h * 64 + 2 * i;
+                    const float p0 = ex2(fmaf(u2f(s[c >> 5][c & 31]), sl2, neg_m));
+                    const float p1 = ex2(fmaf(u2f(s[(c + 1) >> 5][(c + 1) & 31]), sl2, neg_m));
+                    pk[i] = pack_bf16(p0, p1);
+                    ls0 += p0;
+                    ls1 += p1;
+                    lr0 += u2f(pk[i] << 16);
+                    lr1 += u2f(pk[i] & 0xffff0000u);
+                }
+                tmem_st32(tS + h * 32, pk);
+            }
+            l += ls0 + ls1;
+            l_mma += lr0 + lr1;
+            if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                // rescale this warp's 32 rows of O once P_{j-1} V_{j-1} has landed (done after
+                // P_j is written so the S registers are dead; P_j V_j waits for p_ready)
+                if (!__all_sync(0xffffffffu, mbar_wait(my_o, (j - 1) & 1, wd, kSiteSoftO))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c0, o);
+                    tmem_ld_wait(o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+                    tmem_st32(tO + c0, o);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(my_p);
+        }
+
+        // --------------------------------------------------------- epilogue --
+        bool epi = ok && nbt > 0;
+        if (epi) epi = __all_sync(0xffffffffu, mbar_wait(my_o, (nbt - 1) & 1, wd, kSiteEpi));
+        if (epi) {
+            tc_fence_after();
+            const float inv_l = 1.f / l_mma;
+            const int64_t bh_row = static_cast<int64_t>(bh) * N + row;
+            if (O32) {
+                float* dst = p.O32 + bh_row * D;
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c0, o);
+                    tmem_ld_wait(o);
+                    if (row < N) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(dst + c0 + i) =
+                                make_float4(u2f(o[i]) * inv_l, u2f(o[i + 1]) * inv_l,
+                                            u2f(o[i + 2]) * inv_l, u2f(o[i + 3]) * inv_l);
+                    }
+                }
+            } else {
+                uint8_t* stage = smem + (t ? L::kQ1 : L::kQ0);
+#pragma unroll
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + c0, o);
+                    tmem_ld_wait(o);
+                    const int box = c0 / 64;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int chunk = (c0 % 64) / 8 + q;
+                        uint4 v;
+                        v.x = pack_bf16(u2f(o[8 * q + 0]) * inv_l, u2f(o[8 * q + 1]) * inv_l);
+                        v.y = pack_bf16(u2f(o[8 * q + 2]) * inv_l, u2f(o[8 * q + 3]) * inv_l);
+                        v.z = pack_bf16(u2f(o[8 * q + 4]) * inv_l, u2f(o[8 * q + 5]) * inv_l);
+                        v.w = pack_bf16(u2f(o[8 * q + 6]) * inv_l, u2f(o[8 * q + 7]) * inv_l);
+                        *reinterpret_cast<uint4*>(stage + box * L::kBoxBytes + r * 128 +
+                                                  ((chunk ^ (r & 7)) << 4)) = v;
+                    }
+                }
+                fence_async_shared();
+            }
+            if (row < N) p.LSE[bh_row] = (m_used + __log2f(l)) * kLn2;
+        }
+        if (!O32 && nbt > 0) {
+            // every thread of the warpgroup reaches this barrier, even after an abort
+            named_bar_sync(1 + t, 128);
+            if (r == 0 && epi) {
+                const uint32_t src = sbase + (t ? L::kQ1 : L::kQ0);
+                for (int b = 0; b < L::kBoxes; ++b)
+                    tma_store_3d(&tmO, src + b * L::kBoxBytes, b * 64, q_start, bh);
+                bulk_commit();
+                bulk_wait_read<0>();
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown --
+    if (sh.abort_flag) drain_after_abort();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool CAUSAL, bool O32>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+    using L = FwdLayout<D>;
+    CUtensorMap tq, tk, tv, to;
+    if (!make_tile_map(&tq, a.Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.BH, 64, kBM) ||
+        !make_tile_map(&tk, a.K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.BH, 64, kBN) ||
+        !make_tile_map(&tv, a.V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.BH, 64, kBN))
+        return cudaErrorInvalidValue;
+    if (O32) {
+        to = tq;
+    } else if (!make_tile_map(&to, a.O, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.BH, 64, kBM)) {
+        return cudaErrorInvalidValue;
+    }
+    auto kern = fa_fwd_kernel<D, CAUSAL, O32>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
+    if (e != cudaSuccess) return e;
+    FwdParams p;
+    p.LSE = a.LSE;
+    p.O32 = O32 ? static_cast<float*>(a.O) : nullptr;
+    p.N = a.N;
+    p.n_pairs = (a.N + 2 * kBM - 1) / (2 * kBM);
+    p.scale_log2 = a.tau * kLog2e;
+    p.err = a.err;
+    p.wait_limit_ns = a.wait_limit_ns;
+    dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(p.n_pairs));
+    if (a.ev_start) cudaEventRecord(a.ev_start, stream);
+    kern<<<grid, kThreads, L::kDynSmem, stream>>>(tq, tk, tv, to, p);
+    e = cudaGetLastError();
+    if (e == cudaSuccess && a.ev_stop) e = cudaEventRecord(a.ev_stop, stream);
+    return e;
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+    if (a.d == 64) {
+        if (a.causal) return a.o32 ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, true, false>(a, stream);
+        return a.o32 ? launch_fwd_t<64, false, true>(a, stream) : launch_fwd_t<64, false, false>(a, stream);
+    }
+    if (a.causal) return a.o32 ? launch_fwd_t<128, true, true>(a, stream) : launch_fwd_t<128, true, false>(a, stream);
+    return a.o32 ? launch_fwd_t<128, false, true>(a, stream) : launch_fwd_t<128, false, false>(a, stream);
+}
+
+}  // namespace fa

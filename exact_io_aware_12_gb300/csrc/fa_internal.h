@@ -1,0 +1,61 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Arguments of one forward launch (device pointers, validated by the caller).
+struct FwdArgs {
+    const void* Q;
+    const void* K;
+    const void* V;
+    void* O;          // bf16 or fp32 (o32)
+    float* LSE;
+    int BH, N, d;
+    float tau;
+    bool causal;
+    bool o32;
+    unsigned int* err;
+    unsigned long long wait_limit_ns;
+    cudaEvent_t ev_start;  // optional: recorded around the kernel
+    cudaEvent_t ev_stop;
+};
+
+// Arguments of one backward launch sequence.
+struct BwdArgs {
+    const void* Q;
+    const void* K;
+    const void* V;
+    const void* O;
+    const void* dO;
+    const float* LSE;
+    void* dQ;
+    void* dK;
+    void* dV;
+    float* D;       // workspace: fp32 [BH*N]
+    float* dQacc;   // workspace: fp32 [BH*N*d]
+    int BH, N, d;
+    float tau;
+    bool causal;
+    unsigned int* err;
+    unsigned long long wait_limit_ns;
+    cudaEvent_t ev_start;  // optional: recorded around the main kernel
+    cudaEvent_t ev_stop;
+};
+
+// Encodes a 3-D tiled tensor map over a contiguous [BH][N][cols] tensor with
+// a {box_cols, box_rows, 1} box and the 128-byte swizzle (box_cols * esize
+// must be 128).  Returns false if the driver rejects it.
+bool make_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int esize,
+                   int cols, int rows, int planes, int box_cols, int box_rows);
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_watchdog_selftest(unsigned int* err, unsigned long long limit_ns,
+                                     cudaStream_t stream);
+
+}  // namespace fa

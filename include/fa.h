@@ -1,0 +1,143 @@
+/*
+ * Exact IO-aware attention on GB300 (sm_103a): the C ABI.
+ *
+ * What is computed (tonho.wtf "flash attention" entry, section "como
+ * funciona"; "Atencao eficiente - FlashAttention, sparse e hibrida", sections
+ * "Insight 1 - Tiling" and "Insight 2 - Online softmax"):
+ *
+ *   forward   O = softmax(tau * Q K^T [+ causal mask]) V, computed tile by tile
+ *             with a running row max m and row sum l, so the N x N score
+ *             matrix never reaches device memory; the per-row statistics are
+ *             returned packed as LSE = m + ln l.
+ *   backward  keeps only O and LSE, rebuilds S and P on chip, and uses
+ *             D_i = dO_i . O_i (equal to sum_j P_ij dP_ij) to form
+ *             dS = P o (dP - D); returns dQ, dK, dV.
+ *
+ * Conventions shared by every entry point
+ *   - Q, K, V, O, dO, dQ, dK, dV: bf16, contiguous [B][H][N][d] (d fastest).
+ *     LSE: fp32 [B][H][N], natural log of sum_j exp(tau q_i . k_j).
+ *   - d must be 64 or 128.  N may be any value >= 1 (a ragged last tile is
+ *     handled inside the kernels).  B, H, N, d are ints >= 0; B, H or N equal
+ *     to 0 is an empty problem: FA_OK, nothing is launched, pointers unused.
+ *   - causal = 1 hides key j from query i when j > i (query and key lengths
+ *     are equal, so top-left and bottom-right alignment coincide); 0 = no mask.
+ *   - tau is the score scale, finite and > 0 (usually 1/sqrt(d)).
+ *   - Every pointer is a device pointer (cudaMalloc / PyTorch CUDA memory)
+ *     aligned to 16 bytes.  The caller owns every buffer; the library keeps
+ *     no device allocation between calls.  Outputs must not overlap inputs.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream).  Calls only
+ *     enqueue work on it and never synchronise the host.
+ *   - Errors are returned, never printed: invalid arguments are caught before
+ *     anything is launched.  A kernel whose internal pipeline wait exceeds the
+ *     watchdog limit gives up cleanly and records FA_ERR_TIMEOUT in a device
+ *     word that fa_last_device_error() reads.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, negative size, bad tau, overlap */
+    FA_ERR_UNSUPPORTED = 2,  /* d not in {64, 128}, or no sm_103a device */
+    FA_ERR_WORKSPACE = 3,    /* workspace given but smaller than fa_bwd_workspace_size */
+    FA_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    FA_ERR_TIMEOUT = 5       /* a kernel's bounded pipeline wait ran out */
+} fa_status;
+
+/*
+ * Forward pass.  Reads Q, K, V; writes O (bf16) and LSE (fp32).
+ * Source: tonho.wtf "flash attention", section "como funciona" (scores
+ * tau*Q_i K_j^T, running max and sum, store of O and the statistics).
+ */
+FA_API fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                 int B, int H, int N, int d, float tau, int causal, void* stream);
+
+/*
+ * Forward pass with an fp32 O output (same kernel; only the final store
+ * differs).  For checks whose tolerance is below the bf16 rounding of O.
+ * O: fp32 [B][H][N][d].  Same source as fa_fwd.
+ */
+FA_API fa_status fa_fwd_o32(const void* Q, const void* K, const void* V, float* O, float* LSE,
+                     int B, int H, int N, int d, float tau, int causal, void* stream);
+
+/*
+ * Bytes of device scratch fa_bwd needs: D (fp32 [B][H][N]) and the fp32 dQ
+ * accumulator ([B][H][N][d]), each padded to 256 bytes.  0 for an empty or
+ * unsupported problem.
+ */
+FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass.  Reads Q, K, V, O, dO (bf16) and LSE (fp32, as written by
+ * fa_fwd for the same Q, K, V, tau, causal); writes dQ, dK, dV (bf16; every
+ * element is written, nothing is accumulated into them).
+ * workspace: device scratch of at least fa_bwd_workspace_size() bytes, owned
+ * by the caller and free for the duration of the call on this stream; NULL
+ * asks the library to take it with cudaMallocAsync on the stream and give it
+ * back with cudaFreeAsync after the last kernel.
+ * Source: tonho.wtf "flash attention", section "como funciona", backward
+ * paragraph (keep O and the statistics, rebuild S and P, D_i = dO_i . O_i);
+ * "FlashAttention: O Que E e Como Acelera LLMs na Pratica", pillar 2
+ * (recomputation in the backward pass).
+ */
+FA_API fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV,
+                 void* workspace, size_t workspace_bytes,
+                 int B, int H, int N, int d, float tau, int causal, void* stream);
+
+/* Static, human-readable name of a status code. */
+FA_API const char* fa_status_string(fa_status s);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device error
+ * word for the current device.  FA_ERR_TIMEOUT if some kernel launched since
+ * the last call gave up on a bounded wait, FA_ERR_CUDA if the stream reports
+ * an error, else FA_OK.
+ */
+FA_API fa_status fa_last_device_error(void* stream);
+
+/*
+ * Sets how long (nanoseconds) one pipeline wait inside a kernel may take
+ * before the kernel gives up (default 2e9 = 2 s).  Applies to launches made
+ * after the call, from any thread.  0 restores the default.
+ */
+FA_API fa_status fa_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * Watchdog self-test: launches one small kernel whose barrier wait is never
+ * satisfied, so it times out after `limit_ns` and exits cleanly.  The caller
+ * then sees FA_ERR_TIMEOUT from fa_last_device_error().  No fault, trap or
+ * unbounded wait is involved.
+ */
+FA_API fa_status fa_watchdog_selftest(unsigned long long limit_ns, void* stream);
+
+/*
+ * Kernel timing hook.  With both events non-NULL (cudaEvent_t created by the
+ * caller), every later fa_fwd / fa_fwd_o32 / fa_bwd call made from the
+ * calling host thread records `start` on its stream right before the
+ * attention kernel proper (the forward kernel; the backward's main kernel,
+ * after its D/zeroing pre-kernel) and `stop` right after it, so the caller
+ * can read that kernel's duration with cudaEventElapsedTime.  NULL, NULL
+ * turns it off.  The events stay owned by the caller.  Not part of the
+ * method: a measurement aid.
+ */
+FA_API fa_status fa_set_timing_events(void* start, void* stop);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */
