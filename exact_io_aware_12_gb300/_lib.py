@@ -34,7 +34,11 @@ SIGNATURES = {
     "fa_set_wait_limit_ns": (_I, [_ULL]),
     "fa_watchdog_selftest": (_I, [_ULL, _P]),
     "fa_set_timing_events": (_I, [_P, _P]),
+    "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
 }
+
+# Size of the fixed scratch array fa_bwd_noalloc uses (FA_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib = None
@@ -109,6 +113,13 @@ def fa_watchdog_selftest(limit_ns, stream) -> int:
 
 def fa_set_timing_events(start, stop) -> int:
     return _call("fa_set_timing_events", start, stop)
+
+
+def fa_bwd_noalloc(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, tau, causal, stream) -> int:
+    """fa_bwd without any device allocation, for callers that may not allocate
+    while running; its scratch is a fixed array inside the library."""
+    return _call("fa_bwd_noalloc", Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, tau, causal,
+                 stream)
 
 
 def check(code: int, where: str) -> None:

@@ -328,3 +328,54 @@ fa_status fa_watchdog_selftest(unsigned long long limit_ns, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free backward (fa_bwd_noalloc).  The scratch is a fixed array in
+// the device image.  In host code `g_fa_noalloc_scratch` only names a host-side
+// stand-in, so its device address is looked up per device with
+// cudaGetSymbolAddress before it is handed to the kernels.
+static __device__ __align__(256) unsigned char g_fa_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+struct NoAllocScratch {
+    std::once_flag once;
+    void* ptr = nullptr;  // device address on this device, or null if the lookup failed
+};
+NoAllocScratch g_noalloc[fa::kMaxDevices];
+
+// Runs once per device, with that device current (the caller's current device).
+void* noalloc_scratch_for_current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= fa::kMaxDevices) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    NoAllocScratch& ns = g_noalloc[dev];
+    std::call_once(ns.once, [&ns] {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fa_noalloc_scratch) == cudaSuccess) {
+            ns.ptr = p;
+        } else {
+            cudaGetLastError();
+        }
+    });
+    return ns.ptr;
+}
+}  // namespace
+
+extern "C" fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                                    const void* dO, const float* LSE, void* dQ, void* dK,
+                                    void* dV, int B, int H, int N, int d, float tau, int causal,
+                                    void* stream) {
+    bool empty = false;
+    const fa_status s = fa::check_shape(B, H, N, d, tau, causal, &empty);
+    if (s != FA_OK || empty) return s;
+    // the one limit of this entry point: the problem's scratch must fit the array
+    if (fa_bwd_workspace_size(B, H, N, d) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+    void* scratch = noalloc_scratch_for_current_device();
+    if (scratch == nullptr) return FA_ERR_CUDA;
+    // fa_bwd with a caller-provided workspace allocates nothing
+    return fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, scratch, FA_NOALLOC_SCRATCH_BYTES, B, H, N, d,
+                  tau, causal, stream);
+}
+

@@ -136,6 +136,37 @@ FA_API fa_status fa_watchdog_selftest(unsigned long long limit_ns, void* stream)
  */
 FA_API fa_status fa_set_timing_events(void* start, void* stop);
 
+/*
+ * Backward pass that allocates nothing.
+ *
+ * The pages have no counterpart for this entry point; it exists for callers
+ * that are not allowed to allocate device memory while they run: hosts that
+ * reserve a fixed memory budget up front and forbid libraries from calling
+ * cudaMalloc or cudaMallocAsync later (inference servers, plugins inside a
+ * framework that owns every allocation, latency-bound loops where an
+ * allocation could stall or fail).  Such a caller cannot pass a NULL
+ * workspace to fa_bwd, and may have no spare buffer to lend it either.
+ *
+ * It computes exactly what fa_bwd computes (same arguments, minus the
+ * workspace), using as scratch a fixed array of FA_NOALLOC_SCRATCH_BYTES that
+ * lives in the library's device image.  Every GPU on which the library is
+ * used holds that array until the process exits.  The problem must satisfy
+ * fa_bwd_workspace_size(B, H, N, d) <= FA_NOALLOC_SCRATCH_BYTES, otherwise
+ * the call returns FA_ERR_WORKSPACE before doing anything.  The call makes no
+ * cudaMalloc/cudaFree (or any other allocating) call.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture begins.  All calls share the one array and it keeps the previous
+ * call's contents (the kernels clear what must start at zero), so two calls
+ * whose work overlaps on the GPU (different streams, or different host
+ * threads, on the same device) race on it and give wrong results: order them.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+FA_API fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                                const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                                int B, int H, int N, int d, float tau, int causal, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
