@@ -112,10 +112,16 @@ def profiled_traffic(kernel: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    """nvidia-smi sampling of SM clocks and throttle reasons; samples are
+    timestamped so the summary covers only the timed window (mark_start /
+    mark_end)."""
 
-    def __init__(self, index: int, period_ms: int = 100):
+    FIELDS = "timestamp," + CLOCK_FIELDS
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 50):
         self.index, self.period_ms, self.proc, self.path = index, period_ms, None, None
+        self.t_start = self.t_end = None
 
     def __enter__(self):
         out_dir = os.path.join(ROOT, "gpurun_out")
@@ -124,17 +130,23 @@ class ClockSampler:
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={CLOCK_FIELDS}",
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", f"-lms={self.period_ms}"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
-            time.sleep(0.3)
+            time.sleep(0.5)
         except (OSError, ValueError):
             self.proc = None
         return self
 
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
     def __exit__(self, *exc):
         if self.proc is not None:
-            time.sleep(0.25)
+            time.sleep(0.3)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -142,31 +154,44 @@ class ClockSampler:
                 self.proc.kill()
             self.fh.close()
 
+    @staticmethod
+    def _parse_time(ts: str):
+        from datetime import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.strptime(ts.strip(), fmt).timestamp()
+            except ValueError:
+                continue
+        return None
+
     def summary(self):
         if self.proc is None or not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm, smax, power, reasons = [], None, [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        samples = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax = float(parts[2])
-                power.append(float(parts[3]))
+                samples.append((self._parse_time(parts[0]), float(parts[2]), float(parts[3]),
+                                float(parts[4]), parts[6:10]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["unsampled"]}
-        # "under load": samples drawing at least half the peak power seen
-        pmax = max(power) if power else 0.0
-        loaded = [s for s, p in zip(sm, power) if p >= 0.5 * pmax] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": pmax}
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        inside = samples
+        if self.t_start is not None and self.t_end is not None and samples[0][0] is not None:
+            inside = [x for x in samples if x[0] is not None and
+                      self.t_start - 0.05 <= x[0] <= self.t_end + 0.05]
+            if not inside:   # window shorter than the sampling period: nearest sample
+                mid = 0.5 * (self.t_start + self.t_end)
+                inside = [min(samples, key=lambda x: abs((x[0] or 0) - mid))]
+        reasons = sorted({n for x in inside for n, v in zip(self.REASONS, x[4])
+                          if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(x[1] for x in inside),
+                "sm_max_mhz": max(x[2] for x in inside), "reasons": reasons,
+                "samples_in_window": len(inside),
+                "power_w_max": max(x[3] for x in inside)}
 
 
 def pick_workload(args):
@@ -233,6 +258,7 @@ def run_ours(args):
     with ClockSampler(local) as clocks:
         barrier(world, dev)
         torch.cuda.synchronize(dev)
+        clocks.mark_start()
         t0 = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(float(i))                      # L2 flush, outside the step events
@@ -244,8 +270,9 @@ def run_ours(args):
             _lib.check(_lib.fa_set_timing_events(None, None), "timing")
             st_e[i].record(stream)
         torch.cuda.synchronize(dev)
-        barrier(world, dev)
         wall = time.perf_counter() - t0
+        clocks.mark_end()
+        barrier(world, dev)
     if api.last_device_error(dev) != _lib.FA_OK:
         raise RuntimeError("kernel watchdog fired during the timed steps")
 
@@ -432,7 +459,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)

@@ -14,17 +14,18 @@
 //             diagonal when causal):
 //               S^T  = K Q_i^T            tcgen05, both operands in smem
 //               dP^T = V dO_i^T           tcgen05
-//               P^T  = exp2(c S^T - log2e LSE_i)   warps 0-3, written back to
+//               P^T  = exp2(c S^T - log2e LSE_i)   warps 0-7, written back to
 //                                         tensor memory as bf16 over S^T
 //               dV  += P^T dO_i           tcgen05, A read from tensor memory
-//               dS^T = P^T o (dP^T - D_i) warps 0-3, to tensor memory (over
+//               dS^T = P^T o (dP^T - D_i) warps 0-7, to tensor memory (over
 //                                         dP^T) and to smem
 //               dK  += dS^T Q_i           tcgen05, A from tensor memory
 //               dQ_i = dS K               tcgen05, A = dS^T from smem
-//             warps 4-7 read dQ_i out of tensor memory and add it into the
-//             fp32 accumulator with TMA bulk reductions (no per-element
-//             atomics); at the end they write dK (scaled by tau) and dV.
-//             warp 8 loads (TMA), warp 9 issues the MMAs.
+//             warps 0-7 (two warpgroups, each half of the query columns)
+//             also read dQ_i out of tensor memory into fp32 smem tiles that
+//             warp 10 adds into the accumulator with TMA bulk reductions (no
+//             per-element atomics); at the end they write dK (scaled by tau)
+//             and dV.  Warp 8 loads (TMA), warp 9 issues the MMAs.
 //   bwd_post  dQ = bf16(tau * accumulator).
 // Tensor memory (512 columns): dV and dK accumulators (d each), S^T (128),
 // dP^T (128); for d = 128 the dQ tile reuses the S^T columns once P^T has
@@ -41,9 +42,10 @@ namespace {
 
 constexpr int kBQ = 128;  // query rows per step
 constexpr int kBK = 128;  // keys per CTA
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kReducerWarp = 10;
 constexpr float kLog2e = 1.44269504088896341f;
 
 template <int D>
@@ -76,6 +78,7 @@ struct BwdBarriers {
     uint64_t ds_ready;
     uint64_t dq_full;
     uint64_t dq_drained;
+    uint64_t dq_staged;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -94,7 +97,7 @@ struct BwdParams {
 enum : uint32_t {
     kSiteProd = 21, kSiteMmaKV = 22, kSiteMmaQ = 23, kSiteMmaP = 24, kSiteMmaDS = 25,
     kSiteMmaDrain = 26, kSiteDsS = 27, kSiteDsQ = 28, kSiteDsDP = 29, kSiteDsDQ = 30,
-    kSiteDrain = 31
+    kSiteDrain = 31, kSiteReduce = 32
 };
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -111,14 +114,17 @@ __device__ __forceinline__ void mma_rows_rows(uint32_t tmem_d, uint32_t a, uint3
 }
 
 // D (+)= A_tmem[128 x 128] B, B an MN-major smem tile [128 rows(K) x N] (N = Dn).
+// A (bf16, packed two per column) holds K-columns 0-63 at tensor-memory columns
+// [0, 32) and K-columns 64-127 at [64, 96): each half is written by its own
+// warpgroup over the fp32 values it has already read.
 template <int Dn>
 __device__ __forceinline__ void mma_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint32_t b,
                                            bool accumulate) {
     constexpr uint32_t id = idesc_bf16(128, Dn, false, true);
 #pragma unroll
     for (int k = 0; k < 128 / 16; ++k)
-        mma_ts(tmem_d, tmem_a + k * 8, sw128_desc(b + k * 2048, 128 * 128, 1024), id,
-               accumulate || k > 0);
+        mma_ts(tmem_d, tmem_a + (k >> 2) * 64 + (k & 3) * 8,
+               sw128_desc(b + k * 2048, 128 * 128, 1024), id, accumulate || k > 0);
 }
 
 // D = A B with A MN-major [128(K) x 128(M)] and B MN-major [128(K) x Dn].
@@ -169,20 +175,22 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const uint32_t bar_ds = smem_addr(&sh.ds_ready);
     const uint32_t bar_dq = smem_addr(&sh.dq_full);
     const uint32_t bar_dr = smem_addr(&sh.dq_drained);
+    const uint32_t bar_sg = smem_addr(&sh.dq_staged);
 
     if (threadIdx.x == 0) {
         sh.abort_flag = 0;
         mbar_init(bar_kv, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar_qf + 8 * s, 32);
-            mbar_init(bar_qe + 8 * s, 2);
+            mbar_init(bar_qe + 8 * s, 2);  // MMA commit + the reducer warp
         }
         mbar_init(bar_s, 1);
         mbar_init(bar_dp, 1);
-        mbar_init(bar_p, 128);
-        mbar_init(bar_ds, 128);
+        mbar_init(bar_p, 256);
+        mbar_init(bar_ds, 256);
         mbar_init(bar_dq, 1);
-        mbar_init(bar_dr, 128);
+        mbar_init(bar_dr, 256);
+        mbar_init(bar_sg, 256);
         mbar_init_fence();
     }
     if (warp == kMmaWarp) {
@@ -273,141 +281,160 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                         break;
                     }
                     tc_fence_after();
-                    mma_rows_rows<D>(tmem + L::kTmDP, sV, stage1 + L::kTile);  // dP^T next
-                    mma_commit(bar_dp);
+                    // S^T first: the next step's P^T work waits on it, while dP^T
+                    // is needed only later (the tensor pipe runs in issue order)
                     if (L::kDQAliasS) {
                         if (!mbar_wait(bar_dr, s & 1, wd, kSiteMmaDrain)) { ok = false; break; }
                         tc_fence_after();
                     }
                     mma_rows_rows<D>(tmem + L::kTmS, sK, stage1);              // S^T next
                     mma_commit(bar_s);
+                    mma_rows_rows<D>(tmem + L::kTmDP, sV, stage1 + L::kTile);  // dP^T next
+                    mma_commit(bar_dp);
                 }
             }
         }
         __syncwarp();
-    } else if (warp < 4) {
-        // ------------------------------------------- P^T and dS^T (keys) --
-        const int k = threadIdx.x;  // key row within the tile = tensor-memory lane
-        const int kg = kv_start + k;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t tS = tmem + lane_off + L::kTmS;
-        const uint32_t tDP = tmem + lane_off + L::kTmDP;
-        const float sl2 = p.scale_log2;
-        uint8_t* ds_row = smem + L::kDS + k * 128;
-        for (int s = 0; s < n_steps; ++s) {
-            const int st = s & 1;
-            const int q_start = (first + s) * kBQ;
-            bool got = mbar_wait(bar_s, s & 1, wd, kSiteDsS) &&
-                       mbar_wait(bar_qf + 8 * st, (s >> 1) & 1, wd, kSiteDsQ);
-            if (!__all_sync(FULL, got)) break;
-            tc_fence_after();
-            const float* l2 = lse2_s + st * 128;
-            const bool diag = CAUSAL && (q_start == kv_start);
-            // P^T = exp2(c S^T - log2e LSE), bf16, over the S^T columns
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                uint32_t sv[32];
-                tmem_ld32(tS + h * 32, sv);
-                tmem_ld_wait(sv);
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int c = h * 32 + 2 * i;
-                    float p0 = ex2(fmaf(u2f(sv[2 * i]), sl2, -l2[c]));
-                    float p1 = ex2(fmaf(u2f(sv[2 * i + 1]), sl2, -l2[c + 1]));
-                    if (diag) {
-                        if (kg > q_start + c) p0 = 0.f;
-                        if (kg > q_start + c + 1) p1 = 0.f;
-                    }
-                    if (kg >= N) p0 = p1 = 0.f;  // key row past a ragged end
-                    pk[i] = pack_bf16(p0, p1);
+    } else if (warp == kReducerWarp) {
+        // ---------------------------------------------------------- reducer --
+        // Adds each step's staged fp32 dQ tiles into the accumulator (TMA bulk
+        // reduce-add) and, once the reads are done, hands the stage back to the
+        // producer; waiting here keeps that wait off the softmax warps' path.
+        if (lane == 0) {
+            bool ok = true;
+            for (int s = 0; s < n_steps; ++s) {
+                const int st = s & 1;
+                if (ok) ok = mbar_wait(bar_sg, s & 1, wd, kSiteReduce);
+                if (ok) {
+                    const uint32_t src = sbase + L::kStage0 + st * L::kStageBytes;
+                    const int q_start = (first + s) * kBQ;
+                    for (int b = 0; b < D / 32; ++b)
+                        tma_reduce_add_3d(&tmdQacc, src + b * L::kBox, b * 32, q_start, bh);
+                    bulk_commit();
+                    bulk_wait_read<0>();
                 }
-                tmem_st16(tS + h * 16, pk);
+                mbar_arrive(bar_qe + 8 * st);
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar_p);
-
-            got = mbar_wait(bar_dp, s & 1, wd, kSiteDsDP);
-            if (got && s > 0) got = mbar_wait(bar_dq, (s - 1) & 1, wd, kSiteDsDQ);  // dS smem free
-            if (!__all_sync(FULL, got)) break;
-            tc_fence_after();
-            const float* dv = dvec_s + st * 128;
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                uint32_t dp[32], pk[16];
-                tmem_ld32(tDP + h * 32, dp);
-                tmem_ld16(tS + h * 16, pk);
-                tmem_ld_wait(dp);
-                tmem_ld_wait(pk);
-                uint32_t ds[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int c = h * 32 + 2 * i;
-                    const float p0 = u2f(pk[i] << 16), p1 = u2f(pk[i] & 0xffff0000u);
-                    ds[i] = pack_bf16(p0 * (u2f(dp[2 * i]) - dv[c]),
-                                      p1 * (u2f(dp[2 * i + 1]) - dv[c + 1]));
-                }
-                tmem_st16(tDP + h * 16, ds);
-                // smem copy for the dQ MMA: row k, queries 32h..32h+31 (4 x 16 bytes)
-                uint8_t* sub = ds_row + (h >> 1) * (128 * 128);
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int chunk = (h & 1) * 4 + q4;
-                    *reinterpret_cast<uint4*>(sub + ((chunk ^ (k & 7)) << 4)) =
-                        make_uint4(ds[4 * q4], ds[4 * q4 + 1], ds[4 * q4 + 2], ds[4 * q4 + 3]);
-                }
-            }
-            fence_async_shared();
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(bar_ds);
         }
+        __syncwarp();
     } else {
-        // ------------------------------- dQ drain and dK/dV epilogue (4-7) --
-        const int r = threadIdx.x - 128;  // query row (dQ) / key row (dK, dV)
+        // ------------------------- warpgroups 0 and 1 (warps 0-3 and 4-7) --
+        // Warpgroup h owns query columns [64h, 64h + 64) of P^T and dS^T, and
+        // d-columns [h D/2, (h + 1) D/2) of the dQ drain and the dK/dV epilogue.
+        // A failed wait poisons the rest of the work (ok = false) but every
+        // thread still reaches every named barrier, so none can be left waiting.
+        const int h = warp >> 2;
+        const int r = threadIdx.x & 127;  // key row (P^T, dS^T, dK, dV) / query row (dQ)
+        const int kg = kv_start + r;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tDQ = tmem + lane_off + L::kTmDQ;
+        const uint32_t tS = tmem + lane_off + L::kTmS + 64 * h;
+        const uint32_t tDP = tmem + lane_off + L::kTmDP + 64 * h;
+        const uint32_t tDQ = tmem + lane_off + L::kTmDQ + h * (D / 2);
+        const float sl2 = p.scale_log2;
+        uint8_t* ds_row = smem + L::kDS + h * (128 * 128) + r * 128;
+        constexpr int kDrainBoxes = D / 64;  // fp32 boxes of 32 columns per warpgroup
         bool ok = true;
         for (int s = 0; s < n_steps; ++s) {
             const int st = s & 1;
             const int q_start = (first + s) * kBQ;
-            // the exit decision must be the same for all 128 threads: they share
-            // the named barrier below
-            if (named_bar_or(3, 128, !mbar_wait(bar_dq, s & 1, wd, kSiteDrain))) {
-                ok = false;
-                break;
+            // P^T = exp2(c S^T - log2e LSE), bf16, over this warpgroup's S^T columns
+            if (ok) ok = __all_sync(FULL, mbar_wait(bar_s, s & 1, wd, kSiteDsS) &&
+                                              mbar_wait(bar_qf + 8 * st, (s >> 1) & 1, wd, kSiteDsQ));
+            if (ok) {
+                tc_fence_after();
+                const float* l2 = lse2_s + st * 128 + 64 * h;
+                const bool diag = CAUSAL && (q_start == kv_start);
+                const int qh = q_start + 64 * h;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t sv[32];
+                    tmem_ld32(tS + 32 * c, sv);
+                    tmem_ld_wait(sv);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int q = 32 * c + 2 * i;
+                        float p0 = ex2(fmaf(u2f(sv[2 * i]), sl2, -l2[q]));
+                        float p1 = ex2(fmaf(u2f(sv[2 * i + 1]), sl2, -l2[q + 1]));
+                        if (diag) {
+                            if (kg > qh + q) p0 = 0.f;
+                            if (kg > qh + q + 1) p1 = 0.f;
+                        }
+                        if (kg >= N) p0 = p1 = 0.f;  // key row past a ragged end
+                        pk[i] = pack_bf16(p0, p1);
+                    }
+                    tmem_st16(tS + 16 * c, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
             }
-            tc_fence_after();
-            uint32_t acc[D / 32][32];
+            mbar_arrive(bar_p);
+
+            // dS^T = P^T o (dP^T - D), to tensor memory (over dP^T) and to smem
+            if (ok) ok = __all_sync(FULL, mbar_wait(bar_dp, s & 1, wd, kSiteDsDP) &&
+                                              (s == 0 || mbar_wait(bar_dq, (s - 1) & 1, wd, kSiteDsDQ)));
+            if (ok) {
+                tc_fence_after();
+                const float* dv = dvec_s + st * 128 + 64 * h;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) tmem_ld32(tDQ + c * 32, acc[c]);
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t dp[32], pk[16];
+                    tmem_ld32(tDP + 32 * c, dp);
+                    tmem_ld16(tS + 16 * c, pk);
+                    tmem_ld_wait(dp);
+                    tmem_ld_wait(pk);
+                    uint32_t ds[16];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) tmem_ld_wait(acc[c]);
-            tc_fence_before();
-            mbar_arrive(bar_dr);
-            // stage Q_i + dO_i (free now) as D/32 fp32 boxes of [128 rows x 32 cols]
+                    for (int i = 0; i < 16; ++i) {
+                        const int q = 32 * c + 2 * i;
+                        const float p0 = u2f(pk[i] << 16), p1 = u2f(pk[i] & 0xffff0000u);
+                        ds[i] = pack_bf16(p0 * (u2f(dp[2 * i]) - dv[q]),
+                                          p1 * (u2f(dp[2 * i + 1]) - dv[q + 1]));
+                    }
+                    tmem_st16(tDP + 16 * c, ds);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int chunk = 4 * c + q4;
+                        *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
+                            make_uint4(ds[4 * q4], ds[4 * q4 + 1], ds[4 * q4 + 2], ds[4 * q4 + 3]);
+                    }
+                }
+                fence_async_shared();
+                tmem_st_wait();
+                tc_fence_before();
+            }
+            mbar_arrive(bar_ds);
+
+            // dQ drain: this warpgroup's D/2 columns -> fp32 tiles -> bulk reduce-add
+            if (ok) ok = __all_sync(FULL, mbar_wait(bar_dq, s & 1, wd, kSiteDrain));
             uint8_t* stage = smem + L::kStage0 + st * L::kStageBytes;
+            if (ok) {
+                tc_fence_after();
+                uint32_t acc[kDrainBoxes][32];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+                for (int b = 0; b < kDrainBoxes; ++b) tmem_ld32(tDQ + 32 * b, acc[b]);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    *reinterpret_cast<uint4*>(stage + c * L::kBox + r * 128 + ((j ^ (r & 7)) << 4)) =
-                        make_uint4(acc[c][4 * j], acc[c][4 * j + 1], acc[c][4 * j + 2],
-                                   acc[c][4 * j + 3]);
+                for (int b = 0; b < kDrainBoxes; ++b) tmem_ld_wait(acc[b]);
+                tc_fence_before();
+                mbar_arrive(bar_dr);
+                // Q_i + dO_i of this step are free now: stage fp32 boxes of [128 x 32]
+#pragma unroll
+                for (int b = 0; b < kDrainBoxes; ++b) {
+                    uint8_t* box = stage + (h * kDrainBoxes + b) * L::kBox + r * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4*>(box + ((j ^ (r & 7)) << 4)) =
+                            make_uint4(acc[b][4 * j], acc[b][4 * j + 1], acc[b][4 * j + 2],
+                                       acc[b][4 * j + 3]);
+                }
+                fence_async_shared();
+            } else {
+                mbar_arrive(bar_dr);
             }
-            fence_async_shared();
-            named_bar_sync(2, 128);
-            if (r == 0) {
-                const uint32_t src = sbase + L::kStage0 + st * L::kStageBytes;
-                for (int c = 0; c < D / 32; ++c)
-                    tma_reduce_add_3d(&tmdQacc, src + c * L::kBox, c * 32, q_start, bh);
-                bulk_commit();
-                bulk_wait_read<0>();
-                mbar_arrive(bar_qe + 8 * st);
-            }
+            mbar_arrive(bar_sg);  // the reducer warp adds the staged tiles into dQ
         }
-        // dK = tau * dK_acc and dV, staged over the K and V tiles (no MMA reads them now)
+        // dK = tau * dK_acc and dV (this warpgroup's D/2 columns), staged over the K
+        // and V tiles, which no MMA reads any more
         if (ok) {
             tc_fence_after();
             const uint32_t tDV = tmem + lane_off + L::kTmDV, tDK = tmem + lane_off + L::kTmDK;
@@ -417,7 +444,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 const float scale = which ? p.tau : 1.f;
                 const uint32_t src = which ? tDK : tDV;
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int cc = 0; cc < D / 2; cc += 32) {
+                    const int c0 = h * (D / 2) + cc;
                     uint32_t o[32];
                     tmem_ld32(src + c0, o);
                     tmem_ld_wait(o);
@@ -437,8 +465,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             }
             fence_async_shared();
         }
-        named_bar_sync(2, 128);
-        if (r == 0 && ok) {
+        named_bar_sync(4, 256);
+        if (threadIdx.x == 0 && ok) {
             for (int b = 0; b < L::kBoxes; ++b) {
                 tma_store_3d(&tmdV, sbase + L::kV + b * L::kBox, b * 64, kv_start, bh);
                 tma_store_3d(&tmdK, sbase + L::kK + b * L::kBox, b * 64, kv_start, bh);
