@@ -102,14 +102,19 @@ enum : uint32_t {
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
+constexpr uint32_t kDescHi = sw128_desc_hi(1024);  // every operand tile: 8-row groups 1 KB apart
+constexpr uint32_t kLboMN = 128 * 128;               // MN-major: next 64-element column chunk
+
 // D = A B^T, both K-major tiles of 128 rows x Dk (two 64-column boxes when Dk = 128).
+// a_lo / b_lo: low descriptor halves (K-major) of the tiles.
 template <int Dk>
-__device__ __forceinline__ void mma_rows_rows(uint32_t tmem_d, uint32_t a, uint32_t b) {
+__device__ __forceinline__ void mma_rows_rows(uint32_t tmem_d, uint32_t a_lo, uint32_t b_lo) {
     constexpr uint32_t id = idesc_bf16(128, 128, false, false);
 #pragma unroll
     for (int k = 0; k < Dk / 16; ++k) {
-        const uint32_t off = (k / 4) * (128 * 128) + (k % 4) * 32;
-        mma_ss(tmem_d, sw128_desc(a + off, 16, 1024), sw128_desc(b + off, 16, 1024), id, k > 0);
+        const uint32_t off = ((k / 4) * (128 * 128) + (k % 4) * 32) >> 4;
+        if (k == 0) mma_ss_warp<0>(tmem_d, a_lo + off, b_lo + off, kDescHi, id);
+        else mma_ss_warp<1>(tmem_d, a_lo + off, b_lo + off, kDescHi, id);
     }
 }
 
@@ -118,23 +123,25 @@ __device__ __forceinline__ void mma_rows_rows(uint32_t tmem_d, uint32_t a, uint3
 // [0, 32) and K-columns 64-127 at [64, 96): each half is written by its own
 // warpgroup over the fp32 values it has already read.
 template <int Dn>
-__device__ __forceinline__ void mma_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint32_t b,
+__device__ __forceinline__ void mma_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint32_t b_lo,
                                            bool accumulate) {
     constexpr uint32_t id = idesc_bf16(128, Dn, false, true);
+    if (accumulate) mma_ts_warp<1>(tmem_d, tmem_a, b_lo, kDescHi, id);
+    else mma_ts_warp<0>(tmem_d, tmem_a, b_lo, kDescHi, id);
 #pragma unroll
-    for (int k = 0; k < 128 / 16; ++k)
-        mma_ts(tmem_d, tmem_a + (k >> 2) * 64 + (k & 3) * 8,
-               sw128_desc(b + k * 2048, 128 * 128, 1024), id, accumulate || k > 0);
+    for (int k = 1; k < 128 / 16; ++k)
+        mma_ts_warp<1>(tmem_d, tmem_a + (k >> 2) * 64 + (k & 3) * 8, b_lo + ((k * 2048) >> 4),
+                     kDescHi, id);
 }
 
 // D = A B with A MN-major [128(K) x 128(M)] and B MN-major [128(K) x Dn].
 template <int Dn>
-__device__ __forceinline__ void mma_mn_mn(uint32_t tmem_d, uint32_t a, uint32_t b) {
+__device__ __forceinline__ void mma_mn_mn(uint32_t tmem_d, uint32_t a_lo, uint32_t b_lo) {
     constexpr uint32_t id = idesc_bf16(128, Dn, true, true);
+    mma_ss_warp<0>(tmem_d, a_lo, b_lo, kDescHi, id);
 #pragma unroll
-    for (int k = 0; k < 128 / 16; ++k)
-        mma_ss(tmem_d, sw128_desc(a + k * 2048, 128 * 128, 1024),
-               sw128_desc(b + k * 2048, 128 * 128, 1024), id, k > 0);
+    for (int k = 1; k < 128 / 16; ++k)
+        mma_ss_warp<1>(tmem_d, a_lo + ((k * 2048) >> 4), b_lo + ((k * 2048) >> 4), kDescHi, id);
 }
 
 template <int D, bool CAUSAL>
@@ -229,8 +236,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             for (int e = 0; e < 4; ++e) {
                 const int c = lane * 4 + e;
                 const int q = q_start + c;
-                lse2_s[st * 128 + c] = q < N ? p.LSE[row0 + q] * kLog2e : INFINITY;
-                dvec_s[st * 128 + c] = q < N ? p.Dvec[row0 + q] : 0.f;
+                // stored negated: the softmax warps add them with paired fp32 ops
+                lse2_s[st * 128 + c] = q < N ? -p.LSE[row0 + q] * kLog2e : -INFINITY;
+                dvec_s[st * 128 + c] = q < N ? -p.Dvec[row0 + q] : 0.f;
             }
             const uint32_t stage = sbase + L::kStage0 + st * L::kStageBytes;
             if (lane == 0) {
@@ -246,37 +254,48 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA --
-        if (lane == 0) {
-            const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sDS = sbase + L::kDS;
-            bool ok = mbar_wait(bar_kv, 0, wd, kSiteMmaKV) && mbar_wait(bar_qf, 0, wd, kSiteMmaQ);
+        // The whole warp runs this loop; each MMA and commit is issued by one
+        // elected lane (see mma_ss_warp).
+        {
+            // low descriptor halves: K-major (LBO unused) and MN-major (LBO = 16 KB)
+            const uint32_t k_lo = sw128_desc_lo(sbase + L::kK, 16);
+            const uint32_t k_mn = sw128_desc_lo(sbase + L::kK, kLboMN);
+            const uint32_t v_lo = sw128_desc_lo(sbase + L::kV, 16);
+            const uint32_t ds_mn = sw128_desc_lo(sbase + L::kDS, kLboMN);
+            const uint32_t q_lo0 = sw128_desc_lo(sbase + L::kStage0, 16);
+            const uint32_t q_mn0 = sw128_desc_lo(sbase + L::kStage0, kLboMN);
+            const uint32_t do_lo0 = sw128_desc_lo(sbase + L::kStage0 + L::kTile, 16);
+            const uint32_t do_mn0 = sw128_desc_lo(sbase + L::kStage0 + L::kTile, kLboMN);
+            constexpr uint32_t kStageStep = L::kStageBytes >> 4;
+            bool ok = __all_sync(0xffffffffu, mbar_wait(bar_kv, 0, wd, kSiteMmaKV) &&
+                                                  mbar_wait(bar_qf, 0, wd, kSiteMmaQ));
             if (ok) {
                 tc_fence_after();
-                const uint32_t stage = sbase + L::kStage0;
-                mma_rows_rows<D>(tmem + L::kTmS, sK, stage);              // S^T
-                mma_commit(bar_s);
-                mma_rows_rows<D>(tmem + L::kTmDP, sV, stage + L::kTile);  // dP^T
-                mma_commit(bar_dp);
+                mma_rows_rows<D>(tmem + L::kTmS, k_lo, q_lo0);     // S^T
+                mma_commit_warp(bar_s);
+                mma_rows_rows<D>(tmem + L::kTmDP, v_lo, do_lo0);   // dP^T
+                mma_commit_warp(bar_dp);
             }
             for (int s = 0; ok && s < n_steps; ++s) {
                 const int st = s & 1;
-                const uint32_t stage = sbase + L::kStage0 + st * L::kStageBytes;
-                if (!mbar_wait(bar_p, s & 1, wd, kSiteMmaP)) { ok = false; break; }
+                const uint32_t so = st * kStageStep;
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_p, s & 1, wd, kSiteMmaP))) { ok = false; break; }
                 tc_fence_after();
-                mma_tmem_a<D>(tmem + L::kTmDV, tmem + L::kTmS, stage + L::kTile, s > 0);  // dV
-                if (!mbar_wait(bar_ds, s & 1, wd, kSiteMmaDS)) { ok = false; break; }
+                mma_tmem_a<D>(tmem + L::kTmDV, tmem + L::kTmS, do_mn0 + so, s > 0);   // dV
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_ds, s & 1, wd, kSiteMmaDS))) { ok = false; break; }
                 tc_fence_after();
-                mma_tmem_a<D>(tmem + L::kTmDK, tmem + L::kTmDP, stage, s > 0);            // dK
+                mma_tmem_a<D>(tmem + L::kTmDK, tmem + L::kTmDP, q_mn0 + so, s > 0);   // dK
                 if (!L::kDQAliasS && s > 0) {
-                    if (!mbar_wait(bar_dr, (s - 1) & 1, wd, kSiteMmaDrain)) { ok = false; break; }
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_dr, (s - 1) & 1, wd, kSiteMmaDrain))) { ok = false; break; }
                     tc_fence_after();
                 }
-                mma_mn_mn<D>(tmem + L::kTmDQ, sDS, sK);                                   // dQ
-                mma_commit(bar_dq);
-                mma_commit(bar_qe + 8 * st);
+                mma_mn_mn<D>(tmem + L::kTmDQ, ds_mn, k_mn);                            // dQ
+                mma_commit_warp(bar_dq);
+                mma_commit_warp(bar_qe + 8 * st);
                 if (s + 1 < n_steps) {
                     const int st1 = (s + 1) & 1;
-                    const uint32_t stage1 = sbase + L::kStage0 + st1 * L::kStageBytes;
-                    if (!mbar_wait(bar_qf + 8 * st1, ((s + 1) >> 1) & 1, wd, kSiteMmaQ)) {
+                    const uint32_t so1 = st1 * kStageStep;
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_qf + 8 * st1, ((s + 1) >> 1) & 1, wd, kSiteMmaQ))) {
                         ok = false;
                         break;
                     }
@@ -284,13 +303,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     // S^T first: the next step's P^T work waits on it, while dP^T
                     // is needed only later (the tensor pipe runs in issue order)
                     if (L::kDQAliasS) {
-                        if (!mbar_wait(bar_dr, s & 1, wd, kSiteMmaDrain)) { ok = false; break; }
+                        if (!__all_sync(0xffffffffu, mbar_wait(bar_dr, s & 1, wd, kSiteMmaDrain))) { ok = false; break; }
                         tc_fence_after();
                     }
-                    mma_rows_rows<D>(tmem + L::kTmS, sK, stage1);              // S^T next
-                    mma_commit(bar_s);
-                    mma_rows_rows<D>(tmem + L::kTmDP, sV, stage1 + L::kTile);  // dP^T next
-                    mma_commit(bar_dp);
+                    mma_rows_rows<D>(tmem + L::kTmS, k_lo, q_lo0 + so1);     // S^T next
+                    mma_commit_warp(bar_s);
+                    mma_rows_rows<D>(tmem + L::kTmDP, v_lo, do_lo0 + so1);   // dP^T next
+                    mma_commit_warp(bar_dp);
                 }
             }
         }
@@ -342,9 +361,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                                               mbar_wait(bar_qf + 8 * st, (s >> 1) & 1, wd, kSiteDsQ));
             if (ok) {
                 tc_fence_after();
-                const float* l2 = lse2_s + st * 128 + 64 * h;
+                // -log2(e) LSE per query, pairs of adjacent queries as one 64-bit value
+                const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(lse2_s + st * 128 + 64 * h);
                 const bool diag = CAUSAL && (q_start == kv_start);
                 const int qh = q_start + 64 * h;
+                const uint64_t c2 = f2_pack(sl2, sl2);
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t sv[32];
@@ -354,8 +375,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int q = 32 * c + 2 * i;
-                        float p0 = ex2(fmaf(u2f(sv[2 * i]), sl2, -l2[q]));
-                        float p1 = ex2(fmaf(u2f(sv[2 * i + 1]), sl2, -l2[q + 1]));
+                        const float2 x = f2_unpack(
+                            ffma2(f2_pack(u2f(sv[2 * i]), u2f(sv[2 * i + 1])), c2, nl2[q >> 1]));
+                        float p0 = ex2(x.x);
+                        float p1 = ex2(x.y);
                         if (diag) {
                             if (kg > qh + q) p0 = 0.f;
                             if (kg > qh + q + 1) p1 = 0.f;
@@ -375,7 +398,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                                               (s == 0 || mbar_wait(bar_dq, (s - 1) & 1, wd, kSiteDsDQ)));
             if (ok) {
                 tc_fence_after();
-                const float* dv = dvec_s + st * 128 + 64 * h;
+                // -D per query, pairs of adjacent queries as one 64-bit value
+                const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(dvec_s + st * 128 + 64 * h);
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t dp[32], pk[16];
@@ -387,9 +411,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int q = 32 * c + 2 * i;
-                        const float p0 = u2f(pk[i] << 16), p1 = u2f(pk[i] & 0xffff0000u);
-                        ds[i] = pack_bf16(p0 * (u2f(dp[2 * i]) - dv[q]),
-                                          p1 * (u2f(dp[2 * i + 1]) - dv[q + 1]));
+                        const uint64_t pp = f2_pack(u2f(pk[i] << 16), u2f(pk[i] & 0xffff0000u));
+                        const uint64_t t = fadd2(f2_pack(u2f(dp[2 * i]), u2f(dp[2 * i + 1])), nd2[q >> 1]);
+                        const float2 d = f2_unpack(fmul2(pp, t));
+                        ds[i] = pack_bf16(d.x, d.y);
                     }
                     tmem_st16(tDP + 16 * c, ds);
 #pragma unroll

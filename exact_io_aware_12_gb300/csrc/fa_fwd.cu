@@ -89,26 +89,31 @@ enum : uint32_t {
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
+constexpr uint32_t kDescHi = sw128_desc_hi(1024);  // every operand tile: 8-row groups 1 KB apart
+
+// S = Q K^T: both operands K-major [128 rows x D], D/64 boxes of 64 columns.
+// q_lo / k_lo: low descriptor halves of the tiles' first box.
 template <int D>
-__device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_lo, uint32_t k_lo) {
     constexpr uint32_t id = idesc_bf16(128, 128, false, false);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-        const uint32_t off = (k / 4) * (128 * 128) + (k % 4) * 32;
-        mma_ss(tmem_d, sw128_desc(q_smem + off, 16, 1024), sw128_desc(k_smem + off, 16, 1024), id,
-               k > 0);
+        const uint32_t off = ((k / 4) * (128 * 128) + (k % 4) * 32) >> 4;
+        if (k == 0) mma_ss_warp<0>(tmem_d, q_lo + off, k_lo + off, kDescHi, id);
+        else mma_ss_warp<1>(tmem_d, q_lo + off, k_lo + off, kDescHi, id);
     }
 }
 
+// O += P V: P from tensor memory, V an MN-major [128 keys x D] tile.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_smem,
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_lo,
                                          bool accumulate) {
     constexpr uint32_t id = idesc_bf16(128, D, false, true);
+    if (accumulate) mma_ts_warp<1>(tmem_o, tmem_p, v_lo, kDescHi, id);
+    else mma_ts_warp<0>(tmem_o, tmem_p, v_lo, kDescHi, id);
 #pragma unroll
-    for (int k = 0; k < kBN / 16; ++k) {
-        mma_ts(tmem_o, tmem_p + k * 8, sw128_desc(v_smem + k * 2048, 128 * 128, 1024), id,
-               accumulate || k > 0);
-    }
+    for (int k = 1; k < kBN / 16; ++k)
+        mma_ts_warp<1>(tmem_o, tmem_p + k * 8, v_lo + ((k * 2048) >> 4), kDescHi, id);
 }
 
 template <int D, bool CAUSAL, bool O32>
@@ -198,28 +203,33 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA --
-        if (lane == 0) {
+        // The whole warp runs this loop; each MMA and commit is issued by one
+        // elected lane (see mma_ss_warp).
+        {
             const uint32_t tS[2] = {tmem + L::kTmemS0, tmem + L::kTmemS1};
             const uint32_t tO[2] = {tmem + L::kTmemO0, tmem + L::kTmemO1};
-            const uint32_t sQ[2] = {sbase + L::kQ0, sbase + L::kQ1};
+            const uint32_t qlo[2] = {sw128_desc_lo(sbase + L::kQ0, 16), sw128_desc_lo(sbase + L::kQ1, 16)};
+            const uint32_t klo0 = sw128_desc_lo(sbase + L::kRing, 16);          // K: K-major
+            const uint32_t vlo0 = sw128_desc_lo(sbase + L::kRing, 128 * 128);   // V: MN-major
+            constexpr uint32_t kSlot = L::kTileBytes >> 4;
             const int nblk[2] = {n_blk0, n_blk1};
-            bool ok = mbar_wait(bar_q, 0, wd, kSiteMmaQ) &&
-                      mbar_wait(bar_kv_full, 0, wd, kSiteMmaKV);
+            bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteMmaQ) &&
+                                                  mbar_wait(bar_kv_full, 0, wd, kSiteMmaKV));
             if (ok) {
                 tc_fence_after();
-                const uint32_t k0 = sbase + L::kRing;
                 for (int t = 0; t < 2; ++t) {
                     if (nblk[t] > 0) {
-                        issue_s<D>(tS[t], sQ[t], k0);
-                        mma_commit(bar_s + 8 * t);
+                        issue_s<D>(tS[t], qlo[t], klo0);
+                        mma_commit_warp(bar_s + 8 * t);
                     }
                 }
-                mma_commit(bar_kv_empty);
+                mma_commit_warp(bar_kv_empty);
             }
             for (int j = 0; ok && j < nb; ++j) {
                 const int lv = 2 * j + 1, lk = 2 * j + 2;
                 const int sv = lv % L::kStages, sk = lk % L::kStages;
-                if (!mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1, wd, kSiteMmaKV)) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1, wd, kSiteMmaKV))) {
                     ok = false;
                     break;
                 }
@@ -227,30 +237,31 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 bool k_ready = false;
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (j >= nblk[t]) continue;
-                    if (!mbar_wait(bar_p + 8 * t, j & 1, wd, kSiteMmaP)) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_p + 8 * t, j & 1, wd, kSiteMmaP))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    issue_pv<D>(tO[t], tS[t], sbase + L::kRing + sv * L::kTileBytes, j > 0);
-                    mma_commit(bar_o + 8 * t);
+                    issue_pv<D>(tO[t], tS[t], vlo0 + sv * kSlot, j > 0);
+                    mma_commit_warp(bar_o + 8 * t);
                     if (j + 1 < nblk[t]) {
                         if (!k_ready) {
-                            if (!mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1, wd,
-                                           kSiteMmaKV)) {
+                            if (!__all_sync(0xffffffffu,
+                                            mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1,
+                                                      wd, kSiteMmaKV))) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
                             k_ready = true;
                         }
-                        issue_s<D>(tS[t], sQ[t], sbase + L::kRing + sk * L::kTileBytes);
-                        mma_commit(bar_s + 8 * t);
+                        issue_s<D>(tS[t], qlo[t], klo0 + sk * kSlot);
+                        mma_commit_warp(bar_s + 8 * t);
                     }
                 }
                 if (!ok) break;
-                mma_commit(bar_kv_empty + 8 * sv);
-                if (k_ready) mma_commit(bar_kv_empty + 8 * sk);
+                mma_commit_warp(bar_kv_empty + 8 * sv);
+                if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
             }
         }
         __syncwarp();
@@ -296,11 +307,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
             float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                mx0 = fmaxf(mx0, u2f(s[0][c]));
-                mx1 = fmaxf(mx1, u2f(s[1][c]));
-                mx2 = fmaxf(mx2, u2f(s[2][c]));
-                mx3 = fmaxf(mx3, u2f(s[3][c]));
+            for (int c = 0; c < 32; c += 2) {
+                mx0 = fmax3(mx0, u2f(s[0][c]), u2f(s[0][c + 1]));
+                mx1 = fmax3(mx1, u2f(s[1][c]), u2f(s[1][c + 1]));
+                mx2 = fmax3(mx2, u2f(s[2][c]), u2f(s[2][c + 1]));
+                mx3 = fmax3(mx3, u2f(s[3][c]), u2f(s[3][c + 1]));
             }
             const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
             const bool grow = m_cand > m_used + kRescaleThreshold;
@@ -315,6 +326,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // Two row sums: l_mma over the bf16 P values the P.V MMA consumes (it
             // normalises O, so the weights actually applied sum to one) and l over
             // the fp32 values (it gives LSE).
+            // the scale-and-subtract runs as one paired fp32 FMA per two scores
+            const uint64_t c2 = f2_pack(sl2, sl2), nm2 = f2_pack(neg_m, neg_m);
             float ls0 = 0.f, ls1 = 0.f, lr0 = 0.f, lr1 = 0.f;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -322,8 +335,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int c = h * 64 + 2 * i;
-                    const float p0 = ex2(fmaf(u2f(s[c >> 5][c & 31]), sl2, neg_m));
-                    const float p1 = ex2(fmaf(u2f(s[(c + 1) >> 5][(c + 1) & 31]), sl2, neg_m));
+                    const float2 x = f2_unpack(ffma2(
+                        f2_pack(u2f(s[c >> 5][c & 31]), u2f(s[c >> 5][(c & 31) + 1])), c2, nm2));
+                    const float p0 = ex2(x.x), p1 = ex2(x.y);
                     pk[i] = pack_bf16(p0, p1);
                     ls0 += p0;
                     ls1 += p1;

@@ -260,6 +260,93 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// Cheap issue path.  A single thread issues every MMA, so each instruction
+// on that path costs its full latency: the descriptors are kept as two 32-bit
+// halves, the high half (SBO, version, swizzle) is fixed per layout and the low
+// half (start address, LBO) gets a constant K-step offset with one 32-bit add;
+// the accumulate flag is an immediate.
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr, uint32_t lbo) {
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t sw128_desc_hi(uint32_t sbo) {
+    return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+
+template <int ACC>
+__device__ __forceinline__ void mma_ss_lh(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                          uint32_t idesc) {
+    asm volatile(
+        "{\n"
+        " .reg .b64 da, db;\n"
+        " mov.b64 da, {%1, %3};\n"
+        " mov.b64 db, {%2, %3};\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, %5;\n"
+        "}\n"
+        ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC)
+        : "memory");
+}
+
+template <int ACC>
+__device__ __forceinline__ void mma_ts_lh(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                          uint32_t idesc) {
+    asm volatile(
+        "{\n"
+        " .reg .b64 db;\n"
+        " mov.b64 db, {%2, %3};\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, %5;\n"
+        "}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC)
+        : "memory");
+}
+
+// Warp-wide issue: all 32 lanes execute these (with identical, warp-uniform
+// operands, so the compiler keeps them in uniform registers) and elect.sync
+// picks one lane to issue the instruction.  A lone lane issuing under
+// `if (lane == 0)` needs several issue slots per MMA and starves when busy
+// warps share its scheduler.  The elected lane is the same on every call
+// (full mask, all lanes active), so the MMAs and the commits that track them
+// come from one thread.
+template <int ACC>
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                            uint32_t idesc) {
+    asm volatile(
+        "{\n"
+        " .reg .b64 da, db;\n"
+        " .reg .pred e;\n"
+        " mov.b64 da, {%1, %3};\n"
+        " mov.b64 db, {%2, %3};\n"
+        " elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, %5;\n"
+        "}\n"
+        ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC)
+        : "memory");
+}
+
+template <int ACC>
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                            uint32_t idesc) {
+    asm volatile(
+        "{\n"
+        " .reg .b64 db;\n"
+        " .reg .pred e;\n"
+        " mov.b64 db, {%2, %3};\n"
+        " elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, %5;\n"
+        "}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
+    asm volatile(
+        "{\n"
+        " .reg .pred e;\n"
+        " elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+        "}\n"
+        ::"r"(bar) : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
@@ -361,6 +448,41 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// ----------------------------------------------- paired fp32 arithmetic ----
+// sm_100+ executes one f32x2 instruction for two fp32 lanes held in a 64-bit
+// register pair (element 0 in the low half).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 }  // namespace fa
