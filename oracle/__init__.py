@@ -74,6 +74,16 @@ def _load():
         lib.ora_attn_bwd.restype = None
         lib.ora_attn_bwd.argtypes = [dp, dp, dp, dp, i64, i64, i64, ctypes.c_double,
                                      ctypes.c_int, dp, dp, dp, dp, dp, dp]
+        lib.ora_attn_probs_window.restype = None
+        lib.ora_attn_probs_window.argtypes = [dp, dp, dp, i64, i64, i64, ctypes.c_double, i64, dp]
+        lib.ora_attn_fwd_window.restype = None
+        lib.ora_attn_fwd_window.argtypes = [dp, dp, dp, i64, i64, i64, ctypes.c_double, i64, dp, dp]
+        lib.ora_attn_fwd_rows_window.restype = None
+        lib.ora_attn_fwd_rows_window.argtypes = [dp, dp, dp, i64, i64, i64, ctypes.c_double, i64,
+                                                 lp, i64, dp, dp]
+        lib.ora_attn_bwd_window.restype = None
+        lib.ora_attn_bwd_window.argtypes = [dp, dp, dp, dp, i64, i64, i64, ctypes.c_double, i64,
+                                            dp, dp, dp, dp, dp, dp]
         _lib = lib
         return lib
 
@@ -105,27 +115,46 @@ def set_num_threads(n: int) -> None:
     _load().ora_set_num_threads(int(n))
 
 
-def probs(q, k, v, tau: float, causal: bool) -> np.ndarray:
+def _window(causal: bool, window):
+    """window=None: no window.  Otherwise the causal sliding window of `window`
+    keys (key j visible from query i iff i - window < j <= i)."""
+    if window is None:
+        return None
+    if not causal or int(window) < 1:
+        raise ValueError("a window needs causal=True and window >= 1")
+    return int(window)
+
+
+def probs(q, k, v, tau: float, causal: bool, window=None) -> np.ndarray:
     """Attention probabilities P, shape [..., N, N]."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     BH, N, d = _dims(q)
     P = np.empty(q.shape[:-1] + (N,), dtype=np.float64)
-    _load().ora_attn_probs(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), int(causal), _ptr(P))
+    w = _window(causal, window)
+    if w is None:
+        _load().ora_attn_probs(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), int(causal), _ptr(P))
+    else:
+        _load().ora_attn_probs_window(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), w, _ptr(P))
     return P
 
 
-def fwd(q, k, v, tau: float, causal: bool):
+def fwd(q, k, v, tau: float, causal: bool, window=None):
     """Full forward: returns (O [..., N, d], LSE [..., N])."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     BH, N, d = _dims(q)
     O = np.empty_like(q)
     L = np.empty(q.shape[:-1], dtype=np.float64)
-    _load().ora_attn_fwd(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), int(causal),
-                         _ptr(O), _ptr(L))
+    w = _window(causal, window)
+    if w is None:
+        _load().ora_attn_fwd(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), int(causal),
+                             _ptr(O), _ptr(L))
+    else:
+        _load().ora_attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), w,
+                                    _ptr(O), _ptr(L))
     return O, L
 
 
-def fwd_rows(q, k, v, tau: float, causal: bool, rows):
+def fwd_rows(q, k, v, tau: float, causal: bool, rows, window=None):
     """Forward on selected rows.
 
     ``rows`` holds flat row ids ``bh * N + i``.  Returns (O_rows [n, d],
@@ -138,13 +167,18 @@ def fwd_rows(q, k, v, tau: float, causal: bool, rows):
         raise ValueError("row id out of range")
     O = np.empty((r.size, d), dtype=np.float64)
     L = np.empty((r.size,), dtype=np.float64)
-    _load().ora_attn_fwd_rows(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), int(causal),
-                              r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), r.size,
-                              _ptr(O), _ptr(L))
+    rp = r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    w = _window(causal, window)
+    if w is None:
+        _load().ora_attn_fwd_rows(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), int(causal),
+                                  rp, r.size, _ptr(O), _ptr(L))
+    else:
+        _load().ora_attn_fwd_rows_window(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), w,
+                                         rp, r.size, _ptr(O), _ptr(L))
     return O, L
 
 
-def bwd(q, k, v, do, tau: float, causal: bool, want_fwd: bool = False):
+def bwd(q, k, v, do, tau: float, causal: bool, want_fwd: bool = False, window=None):
     """Analytic backward.  Returns (dQ, dK, dV) or, with ``want_fwd``,
     (dQ, dK, dV, O, LSE, D) where D is the softmax-Jacobian row sum."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
@@ -158,8 +192,13 @@ def bwd(q, k, v, do, tau: float, causal: bool, want_fwd: bool = False):
         po, pl, pd = _ptr(O), _ptr(L), _ptr(D)
     else:
         po = pl = pd = null
-    _load().ora_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), BH, N, d, float(tau),
-                         int(causal), _ptr(dQ), _ptr(dK), _ptr(dV), po, pl, pd)
+    w = _window(causal, window)
+    if w is None:
+        _load().ora_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), BH, N, d, float(tau),
+                             int(causal), _ptr(dQ), _ptr(dK), _ptr(dV), po, pl, pd)
+    else:
+        _load().ora_attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(do), BH, N, d, float(tau), w,
+                                    _ptr(dQ), _ptr(dK), _ptr(dV), po, pl, pd)
     if want_fwd:
         return dQ, dK, dV, O, L, D
     return dQ, dK, dV

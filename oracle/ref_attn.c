@@ -29,6 +29,11 @@
  * Readings where the pages are silent:
  *   - causal: key j is visible from query i iff j <= i (equal query and key
  *     lengths, so top-left and bottom-right alignment coincide);
+ *   - sliding window of w keys ("Atencao eficiente - FlashAttention, sparse e
+ *     hibrida", section "Atencao hibrida: local + global intercalados": local
+ *     layers attend within a window of the most recent tokens): key j is
+ *     visible from query i iff i - w < j <= i, so w counts the query's own key;
+ *     w >= N is plain causal attention;
  *   - LSE is in natural-log units of the tau-scaled scores;
  *   - the backward is the analytic gradient of O with respect to Q, K, V for
  *     an upstream gradient dO, with the softmax Jacobian written out as
@@ -49,10 +54,10 @@
 #include <omp.h>
 #endif
 
-/* Key j is visible from query i. */
-static int visible(int64_t i, int64_t j, int causal)
+/* Key j is visible from query i (window > 0: only the `window` most recent keys). */
+static int visible(int64_t i, int64_t j, int causal, int64_t window)
 {
-    return !causal || j <= i;
+    return (!causal || j <= i) && (window <= 0 || j > i - window);
 }
 
 static double dot(const double* a, const double* b, int64_t d)
@@ -72,19 +77,19 @@ static double dot(const double* a, const double* b, int64_t d)
  *   lse   : m + ln l
  */
 static void row_forward(const double* q, const double* K, const double* V,
-                        int64_t i, int64_t N, int64_t d, double tau, int causal,
+                        int64_t i, int64_t N, int64_t d, double tau, int causal, int64_t window,
                         double* p, double* o, double* lse)
 {
     double m = -INFINITY;
     for (int64_t j = 0; j < N; ++j) {
-        if (visible(i, j, causal)) {
+        if (visible(i, j, causal, window)) {
             p[j] = tau * dot(q, K + j * d, d);
             if (p[j] > m) m = p[j];
         }
     }
     double l = 0.0;
     for (int64_t j = 0; j < N; ++j) {
-        if (visible(i, j, causal)) {
+        if (visible(i, j, causal, window)) {
             p[j] = exp(p[j] - m);
             l += p[j];
         } else {
@@ -124,9 +129,9 @@ void ora_set_num_threads(int n)
  * The attention probabilities P [BH][N][N] (row i is the softmax of the
  * visible scaled scores of query i; hidden keys get 0).  For small checks.
  */
-void ora_attn_probs(const double* Q, const double* K, const double* V,
-                    int64_t BH, int64_t N, int64_t d, double tau, int causal,
-                    double* P)
+static void attn_probs(const double* Q, const double* K, const double* V,
+                       int64_t BH, int64_t N, int64_t d, double tau, int causal,
+                       int64_t window, double* P)
 {
     int64_t rows = BH * N;
 #pragma omp parallel
@@ -137,16 +142,16 @@ void ora_attn_probs(const double* Q, const double* K, const double* V,
             int64_t bh = r / N, i = r % N;
             double lse;
             row_forward(Q + r * d, K + bh * N * d, V + bh * N * d, i, N, d, tau,
-                        causal, P + r * N, o, &lse);
+                        causal, window, P + r * N, o, &lse);
         }
         free(o);
     }
 }
 
 /* Forward pass over every row: O [BH][N][d], LSE [BH][N]. */
-void ora_attn_fwd(const double* Q, const double* K, const double* V,
-                  int64_t BH, int64_t N, int64_t d, double tau, int causal,
-                  double* O, double* LSE)
+static void attn_fwd(const double* Q, const double* K, const double* V,
+                     int64_t BH, int64_t N, int64_t d, double tau, int causal,
+                     int64_t window, double* O, double* LSE)
 {
     int64_t rows = BH * N;
 #pragma omp parallel
@@ -156,7 +161,7 @@ void ora_attn_fwd(const double* Q, const double* K, const double* V,
         for (int64_t r = 0; r < rows; ++r) {
             int64_t bh = r / N, i = r % N;
             row_forward(Q + r * d, K + bh * N * d, V + bh * N * d, i, N, d, tau,
-                        causal, p, O + r * d, LSE + r);
+                        causal, window, p, O + r * d, LSE + r);
         }
         free(p);
     }
@@ -166,10 +171,10 @@ void ora_attn_fwd(const double* Q, const double* K, const double* V,
  * Forward pass on a chosen set of rows.  rows[k] = bh * N + i names query i of
  * head bh; outputs O_rows [nrows][d] and LSE_rows [nrows] in the same order.
  */
-void ora_attn_fwd_rows(const double* Q, const double* K, const double* V,
-                       int64_t BH, int64_t N, int64_t d, double tau, int causal,
-                       const int64_t* rows, int64_t nrows,
-                       double* O_rows, double* LSE_rows)
+static void attn_fwd_rows(const double* Q, const double* K, const double* V,
+                          int64_t BH, int64_t N, int64_t d, double tau, int causal,
+                          int64_t window, const int64_t* rows, int64_t nrows,
+                          double* O_rows, double* LSE_rows)
 {
     (void)BH;
 #pragma omp parallel
@@ -180,7 +185,7 @@ void ora_attn_fwd_rows(const double* Q, const double* K, const double* V,
             int64_t r = rows[k];
             int64_t bh = r / N, i = r % N;
             row_forward(Q + r * d, K + bh * N * d, V + bh * N * d, i, N, d, tau,
-                        causal, p, O_rows + k * d, LSE_rows + k);
+                        causal, window, p, O_rows + k * d, LSE_rows + k);
         }
         free(p);
     }
@@ -201,11 +206,11 @@ void ora_attn_fwd_rows(const double* Q, const double* K, const double* V,
  * LSE_out and D_out are optional extra outputs (pass NULL to skip); D_out is
  * the softmax-Jacobian row sum above, so a test can hold it against dO_i . O_i.
  */
-void ora_attn_bwd(const double* Q, const double* K, const double* V,
-                  const double* dO,
-                  int64_t BH, int64_t N, int64_t d, double tau, int causal,
-                  double* dQ, double* dK, double* dV,
-                  double* O_out, double* LSE_out, double* D_out)
+static void attn_bwd(const double* Q, const double* K, const double* V,
+                     const double* dO,
+                     int64_t BH, int64_t N, int64_t d, double tau, int causal, int64_t window,
+                     double* dQ, double* dK, double* dV,
+                     double* O_out, double* LSE_out, double* D_out)
 {
 #pragma omp parallel
     {
@@ -225,7 +230,7 @@ void ora_attn_bwd(const double* Q, const double* K, const double* V,
             /* forward: P and (optionally) O, LSE */
             for (int64_t i = 0; i < N; ++i) {
                 double lse;
-                row_forward(Qh + i * d, Kh, Vh, i, N, d, tau, causal,
+                row_forward(Qh + i * d, Kh, Vh, i, N, d, tau, causal, window,
                             P + i * N, o, &lse);
                 if (O_out) memcpy(O_out + (bh * N + i) * d, o, sizeof(double) * (size_t)d);
                 if (LSE_out) LSE_out[bh * N + i] = lse;
@@ -236,7 +241,7 @@ void ora_attn_bwd(const double* Q, const double* K, const double* V,
                 const double* Pi = P + i * N;
                 double Di = 0.0;
                 for (int64_t j = 0; j < N; ++j) {
-                    dSi[j] = visible(i, j, causal) ? dot(dOh + i * d, Vh + j * d, d) : 0.0;
+                    dSi[j] = visible(i, j, causal, window) ? dot(dOh + i * d, Vh + j * d, d) : 0.0;
                     Di += Pi[j] * dSi[j];
                 }
                 for (int64_t j = 0; j < N; ++j) dSi[j] = Pi[j] * (dSi[j] - Di);
@@ -272,4 +277,60 @@ void ora_attn_bwd(const double* Q, const double* K, const double* V,
         free(dS);
         free(o);
     }
+}
+
+/* ---------------------------------------------------------------- exports --
+ * Plain entry points (no window) and sliding-window entry points (causal,
+ * key j visible from query i iff i - window < j <= i, window >= 1). */
+void ora_attn_probs(const double* Q, const double* K, const double* V, int64_t BH, int64_t N,
+                    int64_t d, double tau, int causal, double* P)
+{
+    attn_probs(Q, K, V, BH, N, d, tau, causal, 0, P);
+}
+
+void ora_attn_fwd(const double* Q, const double* K, const double* V, int64_t BH, int64_t N,
+                  int64_t d, double tau, int causal, double* O, double* LSE)
+{
+    attn_fwd(Q, K, V, BH, N, d, tau, causal, 0, O, LSE);
+}
+
+void ora_attn_fwd_rows(const double* Q, const double* K, const double* V, int64_t BH, int64_t N,
+                       int64_t d, double tau, int causal, const int64_t* rows, int64_t nrows,
+                       double* O_rows, double* LSE_rows)
+{
+    attn_fwd_rows(Q, K, V, BH, N, d, tau, causal, 0, rows, nrows, O_rows, LSE_rows);
+}
+
+void ora_attn_bwd(const double* Q, const double* K, const double* V, const double* dO,
+                  int64_t BH, int64_t N, int64_t d, double tau, int causal,
+                  double* dQ, double* dK, double* dV, double* O_out, double* LSE_out, double* D_out)
+{
+    attn_bwd(Q, K, V, dO, BH, N, d, tau, causal, 0, dQ, dK, dV, O_out, LSE_out, D_out);
+}
+
+void ora_attn_probs_window(const double* Q, const double* K, const double* V, int64_t BH,
+                           int64_t N, int64_t d, double tau, int64_t window, double* P)
+{
+    attn_probs(Q, K, V, BH, N, d, tau, 1, window, P);
+}
+
+void ora_attn_fwd_window(const double* Q, const double* K, const double* V, int64_t BH, int64_t N,
+                         int64_t d, double tau, int64_t window, double* O, double* LSE)
+{
+    attn_fwd(Q, K, V, BH, N, d, tau, 1, window, O, LSE);
+}
+
+void ora_attn_fwd_rows_window(const double* Q, const double* K, const double* V, int64_t BH,
+                              int64_t N, int64_t d, double tau, int64_t window,
+                              const int64_t* rows, int64_t nrows, double* O_rows, double* LSE_rows)
+{
+    attn_fwd_rows(Q, K, V, BH, N, d, tau, 1, window, rows, nrows, O_rows, LSE_rows);
+}
+
+void ora_attn_bwd_window(const double* Q, const double* K, const double* V, const double* dO,
+                         int64_t BH, int64_t N, int64_t d, double tau, int64_t window,
+                         double* dQ, double* dK, double* dV, double* O_out, double* LSE_out,
+                         double* D_out)
+{
+    attn_bwd(Q, K, V, dO, BH, N, d, tau, 1, window, dQ, dK, dV, O_out, LSE_out, D_out);
 }

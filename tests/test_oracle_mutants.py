@@ -13,11 +13,14 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "ref_attn.c")
+PIN_FILES = [os.path.join(ROOT, "tests", f) for f in ("test_oracle_pins.py", "test_oracle_window_pins.py")]
 
 MUTANTS = {
     "scores_without_tau": ("p[j] = tau * dot(q, K + j * d, d);", "p[j] = dot(q, K + j * d, d);"),
-    "causal_mask_reversed": ("return !causal || j <= i;", "return !causal || j >= i;"),
-    "causal_mask_strict": ("return !causal || j <= i;", "return !causal || j < i || i == 0;"),
+    "causal_mask_reversed": ("(!causal || j <= i)", "(!causal || j >= i)"),
+    "causal_mask_strict": ("(!causal || j <= i)", "(!causal || j < i || i == 0)"),
+    "window_off_by_one": ("(window <= 0 || j > i - window)", "(window <= 0 || j >= i - window)"),
+    "window_ignored": ("(window <= 0 || j > i - window)", "(window <= 0 || j > i - 2 * window)"),
     "lse_without_max": ("*lse = m + log(l);", "*lse = log(l);"),
     "no_normalisation": ("for (int64_t j = 0; j < N; ++j) p[j] /= l;", ""),
     "output_wrong_value_row": ("const double* v = V + j * d;", "const double* v = V + (N - 1 - j) * d;"),
@@ -46,8 +49,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
                            "-o", str(lib), str(cfile), "-lm"])
     env = dict(os.environ, FA_ORACLE_LIB=str(lib), OMP_NUM_THREADS="2")
-    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider"] + PIN_FILES,
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
 
@@ -58,7 +60,6 @@ def test_unmutated_copy_passes(tmp_path):
     subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
                            "-o", str(lib), str(tmp_path / "ref_attn_copy.c"), "-lm"])
     env = dict(os.environ, FA_ORACLE_LIB=str(lib), OMP_NUM_THREADS="2")
-    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider"] + PIN_FILES,
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-2000:]

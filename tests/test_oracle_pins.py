@@ -36,8 +36,9 @@ def _arr(x):
 def _golden_cases():
     doc = json.load(open(os.path.join(HERE, "golden", "hand_worked.json")))
     for case in doc["cases"]:
-        for mode in ("noncausal", "causal"):
-            yield pytest.param(case, mode, id=f"{case['name']}-{mode}")
+        for mode in ("noncausal", "causal", "windowed"):
+            if mode in case:
+                yield pytest.param(case, mode, id=f"{case['name']}-{mode}")
 
 
 @pytest.mark.parametrize("case,mode", list(_golden_cases()))
@@ -45,11 +46,12 @@ def test_golden_hand_worked(case, mode):
     q, k, v, do = (_arr(case[n])[None] for n in ("q", "k", "v", "do"))
     tau = _expr(case["tau"])
     exp = case[mode]
-    causal = mode == "causal"
-    O, L = oracle.fwd(q, k, v, tau, causal)
+    causal = mode in ("causal", "windowed")
+    window = int(_expr(case["window"])) if mode == "windowed" else None
+    O, L = oracle.fwd(q, k, v, tau, causal, window=window)
     np.testing.assert_allclose(O[0], _arr(exp["o"]), rtol=0, atol=1e-12)
     np.testing.assert_allclose(L[0], _arr(exp["lse"]), rtol=0, atol=1e-12)
-    dq, dk, dv, O2, L2, D = oracle.bwd(q, k, v, do, tau, causal, want_fwd=True)
+    dq, dk, dv, O2, L2, D = oracle.bwd(q, k, v, do, tau, causal, want_fwd=True, window=window)
     np.testing.assert_allclose(dq[0], _arr(exp["dq"]), rtol=0, atol=1e-12)
     np.testing.assert_allclose(dk[0], _arr(exp["dk"]), rtol=0, atol=1e-12)
     np.testing.assert_allclose(dv[0], _arr(exp["dv"]), rtol=0, atol=1e-12)
