@@ -299,6 +299,8 @@ def run_ours(args):
                 "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
                 "traffic": profiled_traffic(dom_name)}
 
+    window_leg = (measure_window(w, q, k, v, do, dev, args.window, min(args.steps, 20), peak)
+                  if args.window > 0 and w.causal else None)
     e2e = run_e2e(args, w, x, dev, f_step) if not args.no_e2e else None
     cpu = run_cpu_baseline(w, budget_s=args.cpu_seconds) if (rank == 0 and not args.no_cpu) else None
 
@@ -324,6 +326,7 @@ def run_ours(args):
                             "frac": round(bwdk_tf / peak, 4)},
         "fwd_bwd_step": {"ms": round(step_avg_ms, 4), "tflops_per_gpu": round(value / world, 2)},
         "roofline": roofline,
+        "sliding_window": window_leg,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 4 * args.steps,
@@ -334,6 +337,56 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def window_flops_fwd(B, H, N, d, window):
+    """Counted forward FLOPs with a causal window: 4 d per visible score, and row
+    i sees min(i + 1, window) keys."""
+    n_in = min(N, window)
+    visible = n_in * (n_in + 1) // 2 + (N - n_in) * window
+    return 4.0 * B * H * d * visible
+
+
+def measure_window(w, q, k, v, do, dev, window, steps, peak):
+    """The same workload with a causal sliding window (fa_fwd_window /
+    fa_bwd_window): per-kernel CUDA-event times and TFLOP/s on the window's
+    counted FLOPs (backward = 2.5 x forward)."""
+    import torch
+    from exact_io_aware_12_gb300 import api, _lib
+
+    B, H, N, d = w.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    ws = torch.empty(api.workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        api.fwd(q, k, v, True, w.tau, out=o, lse=lse, window=window)
+        api.bwd(q, k, v, o, do, lse, True, w.tau, dq=dq, dk=dk, dv=dv, workspace=ws, window=window)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for e in sum(ev, []):
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        flush.fill_(float(i))
+        _lib.check(_lib.fa_set_timing_events(ev[i][0].cuda_event, ev[i][1].cuda_event), "timing")
+        api.fwd(q, k, v, True, w.tau, out=o, lse=lse, window=window)
+        _lib.check(_lib.fa_set_timing_events(ev[i][2].cuda_event, ev[i][3].cuda_event), "timing")
+        api.bwd(q, k, v, o, do, lse, True, w.tau, dq=dq, dk=dk, dv=dv, workspace=ws, window=window)
+        _lib.check(_lib.fa_set_timing_events(None, None), "timing")
+    torch.cuda.synchronize(dev)
+    if api.last_device_error(dev) != _lib.FA_OK:
+        raise RuntimeError("kernel watchdog fired in the sliding-window leg")
+    fms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    bms = sum(e[2].elapsed_time(e[3]) for e in ev) / steps
+    ff = window_flops_fwd(B, H, N, d, window)
+    return {"window": window, "steps": steps,
+            "fwd": {"ms": round(fms, 4), "tflops": round(ff / fms / 1e9, 2),
+                    "frac": round(ff / fms / 1e9 / peak, 4)},
+            "bwd_main_kernel": {"ms": round(bms, 4), "tflops": round(2.5 * ff / bms / 1e9, 2),
+                                "frac": round(2.5 * ff / bms / 1e9 / peak, 4)},
+            "flops_fwd": ff}
 
 
 def run_e2e(args, w, x, dev, f_step):
@@ -469,6 +522,8 @@ def main(argv=None):
                     help="CPU time budget of the oracle baseline sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--window", type=int, default=4096,
+                    help="also time the causal sliding-window kernels with this window (0: skip)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -34,6 +34,8 @@ SIGNATURES = {
     "fa_set_wait_limit_ns": (_I, [_ULL]),
     "fa_watchdog_selftest": (_I, [_ULL, _P]),
     "fa_set_timing_events": (_I, [_P, _P]),
+    "fa_fwd_window": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_bwd_window": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
 }
 
@@ -83,6 +85,16 @@ def fa_fwd(Q, K, V, O, LSE, B, H, N, d, tau, causal, stream) -> int:
 
 def fa_fwd_o32(Q, K, V, O, LSE, B, H, N, d, tau, causal, stream) -> int:
     return _call("fa_fwd_o32", Q, K, V, O, LSE, B, H, N, d, tau, causal, stream)
+
+
+def fa_fwd_window(Q, K, V, O, LSE, B, H, N, d, tau, window, stream) -> int:
+    return _call("fa_fwd_window", Q, K, V, O, LSE, B, H, N, d, tau, window, stream)
+
+
+def fa_bwd_window(Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, tau,
+                  window, stream) -> int:
+    return _call("fa_bwd_window", Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B,
+                 H, N, d, tau, window, stream)
 
 
 def fa_bwd_workspace_size(B, H, N, d) -> int:

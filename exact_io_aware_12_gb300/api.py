@@ -33,9 +33,12 @@ def _check_inputs(*ts: torch.Tensor) -> Tuple[int, int, int, int]:
 
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool,
         tau: Optional[float] = None, out: Optional[torch.Tensor] = None,
-        lse: Optional[torch.Tensor] = None, o_fp32: bool = False):
+        lse: Optional[torch.Tensor] = None, o_fp32: bool = False, window: Optional[int] = None):
     """Forward pass.  Returns (O, LSE): O bf16 (fp32 with ``o_fp32``) and LSE
-    fp32 [B, H, N]."""
+    fp32 [B, H, N].  ``window`` (with ``causal``): each query sees only its
+    ``window`` most recent keys (fa_fwd_window)."""
+    if window is not None and (not causal or o_fp32):
+        raise ValueError("a window needs causal=True and a bf16 O")
     B, H, N, d = _check_inputs(q, k, v)
     tau = 1.0 / math.sqrt(d) if tau is None else float(tau)
     o_dtype = torch.float32 if o_fp32 else torch.bfloat16
@@ -43,6 +46,12 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool,
         out = torch.empty(q.shape, dtype=o_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if window is not None:
+        code = _lib.fa_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  lse.data_ptr(), B, H, N, d, tau, int(window),
+                                  _stream_handle(q.device))
+        _lib.check(code, "fa_fwd_window")
+        return out, lse
     fn = _lib.fa_fwd_o32 if o_fp32 else _lib.fa_fwd
     code = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
               B, H, N, d, tau, int(bool(causal)), _stream_handle(q.device))
@@ -56,7 +65,8 @@ def workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 
 def bwd(q, k, v, o, do, lse, causal: bool, tau: Optional[float] = None,
         dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
-        dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+        dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+        window: Optional[int] = None):
     """Backward pass.  Returns (dQ, dK, dV), bf16.  ``workspace`` (a byte
     tensor of at least ``workspace_bytes`` bytes) is allocated with torch when
     not given, so the library itself allocates nothing."""
@@ -70,6 +80,15 @@ def bwd(q, k, v, o, do, lse, causal: bool, tau: Optional[float] = None,
     need = workspace_bytes(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if window is not None:
+        if not causal:
+            raise ValueError("a window needs causal=True")
+        code = _lib.fa_bwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                  dv.data_ptr(), workspace.data_ptr(), workspace.numel(), B, H, N,
+                                  d, tau, int(window), _stream_handle(q.device))
+        _lib.check(code, "fa_bwd_window")
+        return dq, dk, dv
     code = _lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                        workspace.data_ptr(), workspace.numel(), B, H, N, d, tau,

@@ -109,7 +109,7 @@ fa_status check_shape(int B, int H, int N, int d, float tau, int causal, bool* e
 fa_status map_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
 fa_status fwd_common(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
-                     int N, int d, float tau, int causal, void* stream, bool o32) {
+                     int N, int d, float tau, int causal, void* stream, bool o32, int window = 0) {
     bool empty = false;
     fa_status s = check_shape(B, H, N, d, tau, causal, &empty);
     if (s != FA_OK || empty) return s;
@@ -136,6 +136,7 @@ fa_status fwd_common(const void* Q, const void* K, const void* V, void* O, float
     a.d = d;
     a.tau = tau;
     a.causal = causal != 0;
+    a.window = window;
     a.o32 = o32;
     a.err = di->err_word;
     a.wait_limit_ns = g_wait_limit_ns.load();
@@ -206,10 +207,10 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
     return round256(rows * sizeof(float)) + round256(rows * d * sizeof(float));
 }
 
-fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
-                 const float* LSE, void* dQ, void* dK, void* dV, void* workspace,
-                 size_t workspace_bytes, int B, int H, int N, int d, float tau, int causal,
-                 void* stream) {
+static fa_status bwd_common(const void* Q, const void* K, const void* V, const void* O,
+                            const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                            void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                            float tau, int causal, int window, void* stream) {
     bool empty = false;
     fa_status s = check_shape(B, H, N, d, tau, causal, &empty);
     if (s != FA_OK || empty) return s;
@@ -261,6 +262,7 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
     a.d = d;
     a.tau = tau;
     a.causal = causal != 0;
+    a.window = window;
     a.err = di->err_word;
     a.wait_limit_ns = g_wait_limit_ns.load();
     a.ev_start = t_ev_start;
@@ -268,6 +270,29 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
     const cudaError_t e = launch_bwd(a, st);
     if (workspace == nullptr) cudaFreeAsync(ws, st);
     return map_cuda(e);
+}
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV, void* workspace,
+                 size_t workspace_bytes, int B, int H, int N, int d, float tau, int causal,
+                 void* stream) {
+    return bwd_common(Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, tau,
+                      causal, 0, stream);
+}
+
+fa_status fa_fwd_window(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                        int H, int N, int d, float tau, int window, void* stream) {
+    if (window < 1) return FA_ERR_INVALID_ARG;
+    return fwd_common(Q, K, V, O, LSE, B, H, N, d, tau, 1, stream, false, window);
+}
+
+fa_status fa_bwd_window(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                        const float* LSE, void* dQ, void* dK, void* dV, void* workspace,
+                        size_t workspace_bytes, int B, int H, int N, int d, float tau, int window,
+                        void* stream) {
+    if (window < 1) return FA_ERR_INVALID_ARG;
+    return bwd_common(Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, tau,
+                      1, window, stream);
 }
 
 const char* fa_status_string(fa_status s) {

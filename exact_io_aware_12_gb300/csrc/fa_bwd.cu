@@ -88,6 +88,7 @@ struct BwdParams {
     const float* Dvec;
     int N;
     int n_kv;
+    int window;        // causal sliding window in keys (0 = none)
     float scale_log2;  // tau * log2(e)
     float tau;
     unsigned int* err;
@@ -144,7 +145,8 @@ __device__ __forceinline__ void mma_mn_mn(uint32_t tmem_d, uint32_t a_lo, uint32
         mma_ss_warp<1>(tmem_d, a_lo + ((k * 2048) >> 4), b_lo + ((k * 2048) >> 4), kDescHi, id);
 }
 
-template <int D, bool CAUSAL>
+// LOCAL: causal sliding window of p.window keys (only with CAUSAL).
+template <int D, bool CAUSAL, bool LOCAL>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -165,8 +167,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const int N = p.N;
     const int kv_start = kv_tile * kBK;
     const int n_q = (N + kBQ - 1) / kBQ;
+    // Query tiles that see this key tile: from the diagonal when causal, and with
+    // a sliding window only up to the tile holding query (last key + window - 1).
+    const int window = (CAUSAL && LOCAL) ? p.window : 0;
     const int first = CAUSAL ? kv_tile : 0;
-    const int n_steps = n_q - first;
+    const int last = window > 0 ? min(n_q - 1, (kv_start + kBK - 1 + window - 1) / kBQ) : n_q - 1;
+    const int n_steps = last - first + 1;
 
     if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicCAS(p.err, 0u, 1u | (0xAAu << 8));
@@ -364,6 +370,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 // -log2(e) LSE per query, pairs of adjacent queries as one 64-bit value
                 const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(lse2_s + st * 128 + 64 * h);
                 const bool diag = CAUSAL && (q_start == kv_start);
+                // window edge: query q no longer sees key kg once q >= kg + window
+                const bool wedge = window > 0 && q_start + kBQ - 1 >= kv_start + window;
                 const int qh = q_start + 64 * h;
                 const uint64_t c2 = f2_pack(sl2, sl2);
 #pragma unroll
@@ -382,6 +390,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                         if (diag) {
                             if (kg > qh + q) p0 = 0.f;
                             if (kg > qh + q + 1) p1 = 0.f;
+                        }
+                        if constexpr (LOCAL) {
+                            if (wedge) {
+                                if (qh + q >= kg + window) p0 = 0.f;
+                                if (qh + q + 1 >= kg + window) p1 = 0.f;
+                            }
                         }
                         if (kg >= N) p0 = p1 = 0.f;  // key row past a ragged end
                         pk[i] = pack_bf16(p0, p1);
@@ -558,7 +572,7 @@ __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restric
     }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool LOCAL = false>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     using L = BwdLayout<D>;
     const int64_t rows = static_cast<int64_t>(a.BH) * a.N;
@@ -585,7 +599,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
             !make_tile_map(&tdk, a.dK, BF, 2, D, a.N, a.BH, 64, kBK) ||
             !make_tile_map(&tdv, a.dV, BF, 2, D, a.N, a.BH, 64, kBK))
             return cudaErrorInvalidValue;
-        auto kern = fa_bwd_main_kernel<D, CAUSAL>;
+        auto kern = fa_bwd_main_kernel<D, CAUSAL, LOCAL>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
         if (e != cudaSuccess) return e;
         BwdParams p;
@@ -595,6 +609,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         p.n_kv = (a.N + kBK - 1) / kBK;
         p.scale_log2 = a.tau * kLog2e;
         p.tau = a.tau;
+        p.window = (a.window > 0 && a.window < a.N) ? a.window : 0;
         p.err = a.err;
         p.wait_limit_ns = a.wait_limit_ns;
         dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(p.n_kv));
@@ -618,6 +633,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+    if (a.causal && a.window > 0 && a.window < a.N)
+        return a.d == 64 ? launch_bwd_t<64, true, true>(a, stream) : launch_bwd_t<128, true, true>(a, stream);
     if (a.d == 64) return a.causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
     return a.causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
 }

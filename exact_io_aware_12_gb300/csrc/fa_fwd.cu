@@ -67,6 +67,7 @@ struct FwdParams {
     float scale_log2;  // tau * log2(e)
     unsigned int* err;
     unsigned long long wait_limit_ns;
+    int window;  // causal sliding window in keys (0 = none)
 };
 
 struct FwdShared {
@@ -116,7 +117,8 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
         mma_ts_warp<1>(tmem_o, tmem_p + k * 8, v_lo + ((k * 2048) >> 4), kDescHi, id);
 }
 
-template <int D, bool CAUSAL, bool O32>
+// LOCAL: causal sliding window of p.window keys (only with CAUSAL).
+template <int D, bool CAUSAL, bool O32, bool LOCAL>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -137,9 +139,18 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int n_kv = (N + kBN - 1) / kBN;
     const int q_start0 = pair * 2 * kBM;
     const int q_start1 = q_start0 + kBM;
-    int n_blk0 = CAUSAL ? min(n_kv, q_start0 / kBN + 1) : n_kv;
-    int n_blk1 = q_start1 < N ? (CAUSAL ? min(n_kv, q_start1 / kBN + 1) : n_kv) : 0;
-    const int nb = max(n_blk0, n_blk1);
+    // Key blocks [lo_t, hi_t) of tile t: up to the diagonal when causal, and from
+    // the block holding key (first row - window + 1) with a sliding window.  The
+    // two ranges overlap or touch, so the loaders walk [jlo, jhi) without gaps.
+    const int window = (CAUSAL && LOCAL) ? p.window : 0;
+    const int hi0 = CAUSAL ? min(n_kv, q_start0 / kBN + 1) : n_kv;
+    const int hi1 = q_start1 < N ? (CAUSAL ? min(n_kv, q_start1 / kBN + 1) : n_kv) : 0;
+    const int lo0 = window > 0 ? max(0, q_start0 - window + 1) / kBN : 0;
+    const int lo1 = window > 0 ? max(0, q_start1 - window + 1) / kBN : 0;
+    const int n_blk0 = hi0 - lo0;
+    const int n_blk1 = hi1 > 0 ? hi1 - lo1 : 0;
+    const int jlo = lo0;
+    const int nb = max(hi0, hi1) - jlo;  // key blocks loaded
 
     const uint32_t bar_q = smem_addr(&sh.q_full);
     const uint32_t bar_kv_full = smem_addr(&sh.kv_full[0]);
@@ -178,99 +189,150 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t tmem = sh.tmem_base;
     const Watchdog wd{p.err, &sh.abort_flag, p.wait_limit_ns};
 
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------------- producer --
-        if (lane == 0) {
-            uint32_t qbytes = L::kTileBytes * ((n_blk0 > 0) + (n_blk1 > 0));
-            mbar_arrive_expect_tx(bar_q, qbytes);
-            for (int b = 0; b < L::kBoxes; ++b) {
-                tma_load_3d(sbase + L::kQ0 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start0, bh);
-                if (n_blk1 > 0)
-                    tma_load_3d(sbase + L::kQ1 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start1, bh);
-            }
-            for (int ld = 0; ld < 2 * nb; ++ld) {
-                const int slot = ld % L::kStages;
-                if (ld >= L::kStages &&
-                    !mbar_wait(bar_kv_empty + 8 * slot, ((ld / L::kStages) - 1) & 1, wd, kSiteProdEmpty))
-                    break;
-                const CUtensorMap* map = (ld & 1) ? &tmV : &tmK;
-                const uint32_t dst = sbase + L::kRing + slot * L::kTileBytes;
-                mbar_arrive_expect_tx(bar_kv_full + 8 * slot, L::kTileBytes);
-                for (int b = 0; b < L::kBoxes; ++b)
-                    tma_load_3d(dst + b * L::kBoxBytes, map, bar_kv_full + 8 * slot, b * 64,
-                                (ld >> 1) * kBN, bh);
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA --
-        // The whole warp runs this loop; each MMA and commit is issued by one
-        // elected lane (see mma_ss_warp).
-        {
-            const uint32_t tS[2] = {tmem + L::kTmemS0, tmem + L::kTmemS1};
-            const uint32_t tO[2] = {tmem + L::kTmemO0, tmem + L::kTmemO1};
-            const uint32_t qlo[2] = {sw128_desc_lo(sbase + L::kQ0, 16), sw128_desc_lo(sbase + L::kQ1, 16)};
-            const uint32_t klo0 = sw128_desc_lo(sbase + L::kRing, 16);          // K: K-major
-            const uint32_t vlo0 = sw128_desc_lo(sbase + L::kRing, 128 * 128);   // V: MN-major
-            constexpr uint32_t kSlot = L::kTileBytes >> 4;
-            const int nblk[2] = {n_blk0, n_blk1};
-            bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteMmaQ) &&
-                                                  mbar_wait(bar_kv_full, 0, wd, kSiteMmaKV));
-            if (ok) {
-                tc_fence_after();
-                for (int t = 0; t < 2; ++t) {
-                    if (nblk[t] > 0) {
-                        issue_s<D>(tS[t], qlo[t], klo0);
-                        mma_commit_warp(bar_s + 8 * t);
-                    }
+    if (warp >= kProducerWarp) {
+        if (warp == kProducerWarp) {
+            // ------------------------------------------------------- producer --
+            if (lane == 0) {
+                uint32_t qbytes = L::kTileBytes * ((n_blk0 > 0) + (n_blk1 > 0));
+                mbar_arrive_expect_tx(bar_q, qbytes);
+                for (int b = 0; b < L::kBoxes; ++b) {
+                    tma_load_3d(sbase + L::kQ0 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start0, bh);
+                    if (n_blk1 > 0)
+                        tma_load_3d(sbase + L::kQ1 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start1, bh);
                 }
-                mma_commit_warp(bar_kv_empty);
-            }
-            for (int j = 0; ok && j < nb; ++j) {
-                const int lv = 2 * j + 1, lk = 2 * j + 2;
-                const int sv = lv % L::kStages, sk = lk % L::kStages;
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1, wd, kSiteMmaKV))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                bool k_ready = false;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j >= nblk[t]) continue;
-                    if (!__all_sync(0xffffffffu, mbar_wait(bar_p + 8 * t, j & 1, wd, kSiteMmaP))) {
-                        ok = false;
+                for (int ld = 0; ld < 2 * nb; ++ld) {
+                    const int slot = ld % L::kStages;
+                    if (ld >= L::kStages &&
+                        !mbar_wait(bar_kv_empty + 8 * slot, ((ld / L::kStages) - 1) & 1, wd, kSiteProdEmpty))
                         break;
-                    }
+                    const CUtensorMap* map = (ld & 1) ? &tmV : &tmK;
+                    const uint32_t dst = sbase + L::kRing + slot * L::kTileBytes;
+                    mbar_arrive_expect_tx(bar_kv_full + 8 * slot, L::kTileBytes);
+                    for (int b = 0; b < L::kBoxes; ++b)
+                        tma_load_3d(dst + b * L::kBoxBytes, map, bar_kv_full + 8 * slot, b * 64,
+                                    (jlo + (ld >> 1)) * kBN, bh);
+                }
+            }
+        } else if (warp == kMmaWarp) {
+            // ------------------------------------------------------------ MMA --
+            // The whole warp runs this loop; each MMA and commit is issued by one
+            // elected lane (see mma_ss_warp).
+            {
+                const uint32_t tS[2] = {tmem + L::kTmemS0, tmem + L::kTmemS1};
+                const uint32_t tO[2] = {tmem + L::kTmemO0, tmem + L::kTmemO1};
+                const uint32_t qlo[2] = {sw128_desc_lo(sbase + L::kQ0, 16), sw128_desc_lo(sbase + L::kQ1, 16)};
+                const uint32_t klo0 = sw128_desc_lo(sbase + L::kRing, 16);          // K: K-major
+                const uint32_t vlo0 = sw128_desc_lo(sbase + L::kRing, 128 * 128);   // V: MN-major
+                constexpr uint32_t kSlot = L::kTileBytes >> 4;
+                const int lo[2] = {lo0, lo1};
+                const int hi[2] = {hi0, n_blk1 > 0 ? hi1 : 0};
+                bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteMmaQ) &&
+                                                      mbar_wait(bar_kv_full, 0, wd, kSiteMmaKV));
+                if (ok) {
                     tc_fence_after();
-                    issue_pv<D>(tO[t], tS[t], vlo0 + sv * kSlot, j > 0);
-                    mma_commit_warp(bar_o + 8 * t);
-                    if (j + 1 < nblk[t]) {
-                        if (!k_ready) {
-                            if (!__all_sync(0xffffffffu,
-                                            mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1,
-                                                      wd, kSiteMmaKV))) {
+                    for (int t = 0; t < 2; ++t) {
+                        if (lo[t] == jlo && hi[t] > jlo) {
+                            issue_s<D>(tS[t], qlo[t], klo0);
+                            mma_commit_warp(bar_s + 8 * t);
+                        }
+                    }
+                    mma_commit_warp(bar_kv_empty);
+                }
+                if constexpr (!LOCAL) {
+                    // every tile starts at key block 0: tile t takes blocks [0, hi[t])
+                    for (int j = 0; ok && j < nb; ++j) {
+                        const int lv = 2 * j + 1, lk = 2 * j + 2;
+                        const int sv = lv % L::kStages, sk = lk % L::kStages;
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1, wd, kSiteMmaKV))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        bool k_ready = false;
+                        for (int t = 0; t < 2 && ok; ++t) {
+                            if (j >= hi[t]) continue;
+                            if (!__all_sync(0xffffffffu, mbar_wait(bar_p + 8 * t, j & 1, wd, kSiteMmaP))) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
-                            k_ready = true;
+                            issue_pv<D>(tO[t], tS[t], vlo0 + sv * kSlot, j > 0);
+                            mma_commit_warp(bar_o + 8 * t);
+                            if (j + 1 < hi[t]) {
+                                if (!k_ready) {
+                                    if (!__all_sync(0xffffffffu,
+                                                    mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1,
+                                                              wd, kSiteMmaKV))) {
+                                        ok = false;
+                                        break;
+                                    }
+                                    tc_fence_after();
+                                    k_ready = true;
+                                }
+                                issue_s<D>(tS[t], qlo[t], klo0 + sk * kSlot);
+                                mma_commit_warp(bar_s + 8 * t);
+                            }
                         }
-                        issue_s<D>(tS[t], qlo[t], klo0 + sk * kSlot);
-                        mma_commit_warp(bar_s + 8 * t);
+                        if (!ok) break;
+                        mma_commit_warp(bar_kv_empty + 8 * sv);
+                        if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
+                    }
+                } else {
+                    // tile t takes blocks [lo[t], hi[t]); S of a tile's first block may
+                    // be issued while the other tile is still in its leading blocks
+                    for (int u = 0; ok && u < nb; ++u) {
+                        const int j = jlo + u;  // key block
+                        const int lv = 2 * u + 1, lk = 2 * u + 2;
+                        const int sv = lv % L::kStages, sk = lk % L::kStages;
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1, wd, kSiteMmaKV))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        bool k_ready = false;
+                        // fully unrolled over the two tiles so the per-tile arrays stay in registers
+    #pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            if (ok && j >= lo[t] && j < hi[t]) {
+                                ok = __all_sync(0xffffffffu,
+                                                mbar_wait(bar_p + 8 * t, (j - lo[t]) & 1, wd, kSiteMmaP));
+                                if (ok) {
+                                    tc_fence_after();
+                                    issue_pv<D>(tO[t], tS[t], vlo0 + sv * kSlot, j > lo[t]);
+                                    mma_commit_warp(bar_o + 8 * t);
+                                }
+                            }
+                            if (ok && j + 1 >= lo[t] && j + 1 < hi[t]) {
+                                if (!k_ready) {
+                                    ok = __all_sync(0xffffffffu,
+                                                    mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1,
+                                                              wd, kSiteMmaKV));
+                                    if (ok) tc_fence_after();
+                                    k_ready = true;
+                                }
+                                if (ok) {
+                                    issue_s<D>(tS[t], qlo[t], klo0 + sk * kSlot);
+                                    mma_commit_warp(bar_s + 8 * t);
+                                }
+                            }
+                        }
+                        if (!ok) break;
+                        mma_commit_warp(bar_kv_empty + 8 * sv);
+                        if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
                     }
                 }
-                if (!ok) break;
-                mma_commit_warp(bar_kv_empty + 8 * sv);
-                if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
             }
+            __syncwarp();
         }
-        __syncwarp();
     } else {
         // -------------------------------------------------------- softmax --
         const int t = warp >> 2;
         const int r = threadIdx.x & 127;
         const int q_start = t ? q_start1 : q_start0;
         const int nbt = t ? n_blk1 : n_blk0;
+        const int lot = t ? lo1 : lo0;
         const int row = q_start + r;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_off + (t ? L::kTmemS1 : L::kTmemS0);
@@ -280,9 +342,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         float m_used = -INFINITY;
         float l = 0.f, l_mma = 0.f;
         bool ok = true;
-        for (int j = 0; j < nbt; ++j) {
+        for (int jj = 0; jj < nbt; ++jj) {
+            const int j = lot + jj;  // key block
             // wait results are made warp-uniform: tcgen05.ld/st are warp-collective
-            if (!__all_sync(0xffffffffu, mbar_wait(my_s, j & 1, wd, kSiteSoftS))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(my_s, jj & 1, wd, kSiteSoftS))) {
                 ok = false;
                 break;
             }
@@ -298,12 +361,20 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tmem_ld_wait(s[3]);
 
             const int kbase = j * kBN;
-            const bool need_mask = (CAUSAL && kbase + kBN - 1 > q_start) || (kbase + kBN > N);
+            const bool need_mask = (CAUSAL && kbase + kBN - 1 > q_start) || (kbase + kBN > N) ||
+                                   (window > 0 && kbase <= q_start + kBM - 1 - window);
             if (need_mask) {
                 const int last = CAUSAL ? min(row, N - 1) : N - 1;  // last visible key
+                if constexpr (LOCAL) {
+                    const int first = row - window + 1;  // first visible key
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (kbase + c > last) s[c >> 5][c & 31] = f2u(-INFINITY);
+                    for (int c = 0; c < 128; ++c)
+                        if (kbase + c > last || kbase + c < first) s[c >> 5][c & 31] = f2u(-INFINITY);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (kbase + c > last) s[c >> 5][c & 31] = f2u(-INFINITY);
+                }
             }
             float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
@@ -348,10 +419,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
             l += ls0 + ls1;
             l_mma += lr0 + lr1;
-            if (j > 0 && __any_sync(0xffffffffu, grow)) {
+            if (jj > 0 && __any_sync(0xffffffffu, grow)) {
                 // rescale this warp's 32 rows of O once P_{j-1} V_{j-1} has landed (done after
                 // P_j is written so the S registers are dead; P_j V_j waits for p_ready)
-                if (!__all_sync(0xffffffffu, mbar_wait(my_o, (j - 1) & 1, wd, kSiteSoftO))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(my_o, (jj - 1) & 1, wd, kSiteSoftO))) {
                     ok = false;
                     break;
                 }
@@ -440,7 +511,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
 }
 
-template <int D, bool CAUSAL, bool O32>
+template <int D, bool CAUSAL, bool O32, bool LOCAL = false>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     using L = FwdLayout<D>;
     CUtensorMap tq, tk, tv, to;
@@ -453,13 +524,14 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     } else if (!make_tile_map(&to, a.O, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.BH, 64, kBM)) {
         return cudaErrorInvalidValue;
     }
-    auto kern = fa_fwd_kernel<D, CAUSAL, O32>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, O32, LOCAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
     if (e != cudaSuccess) return e;
     FwdParams p;
     p.LSE = a.LSE;
     p.O32 = O32 ? static_cast<float*>(a.O) : nullptr;
     p.N = a.N;
+    p.window = (a.window > 0 && a.window < a.N) ? a.window : 0;
     p.n_pairs = (a.N + 2 * kBM - 1) / (2 * kBM);
     p.scale_log2 = a.tau * kLog2e;
     p.err = a.err;
@@ -475,6 +547,9 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+    if (a.causal && !a.o32 && a.window > 0 && a.window < a.N)
+        return a.d == 64 ? launch_fwd_t<64, true, false, true>(a, stream)
+                         : launch_fwd_t<128, true, false, true>(a, stream);
     if (a.d == 64) {
         if (a.causal) return a.o32 ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, true, false>(a, stream);
         return a.o32 ? launch_fwd_t<64, false, true>(a, stream) : launch_fwd_t<64, false, false>(a, stream);

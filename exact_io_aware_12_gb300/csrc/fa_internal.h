@@ -18,6 +18,7 @@ struct FwdArgs {
     int BH, N, d;
     float tau;
     bool causal;
+    int window;       // causal sliding window in keys (0 = none)
     bool o32;
     unsigned int* err;
     unsigned long long wait_limit_ns;
@@ -41,6 +42,7 @@ struct BwdArgs {
     int BH, N, d;
     float tau;
     bool causal;
+    int window;     // causal sliding window in keys (0 = none)
     unsigned int* err;
     unsigned long long wait_limit_ns;
     cudaEvent_t ev_start;  // optional: recorded around the main kernel

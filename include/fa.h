@@ -125,6 +125,28 @@ FA_API fa_status fa_set_wait_limit_ns(unsigned long long ns);
 FA_API fa_status fa_watchdog_selftest(unsigned long long limit_ns, void* stream);
 
 /*
+ * Sliding-window (local) causal attention, forward.  Key j is visible from
+ * query i iff i - window < j <= i: each query attends to its `window` most
+ * recent keys, itself included ("Atencao eficiente - FlashAttention, sparse e
+ * hibrida", section "Atencao hibrida: local + global intercalados": local
+ * layers with windows of 4096 or 128 tokens).  Same buffers and conventions
+ * as fa_fwd with causal = 1; key blocks outside every row's window are never
+ * loaded.  window >= 1 (else FA_ERR_INVALID_ARG); window >= N is plain causal
+ * attention.
+ */
+FA_API fa_status fa_fwd_window(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                               int B, int H, int N, int d, float tau, int window, void* stream);
+
+/*
+ * Sliding-window backward: fa_bwd for the mask of fa_fwd_window (LSE must come
+ * from fa_fwd_window with the same window).  Same workspace rules as fa_bwd.
+ */
+FA_API fa_status fa_bwd_window(const void* Q, const void* K, const void* V, const void* O,
+                               const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                               void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                               float tau, int window, void* stream);
+
+/*
  * Kernel timing hook.  With both events non-NULL (cudaEvent_t created by the
  * caller), every later fa_fwd / fa_fwd_o32 / fa_bwd call made from the
  * calling host thread records `start` on its stream right before the
