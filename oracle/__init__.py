@@ -12,9 +12,11 @@ that file with gcc, loads it with ctypes and marshals numpy float64 arrays.
 Every function takes arrays shaped ``[BH, N, d]`` (or ``[B, H, N, d]``; only
 the trailing two axes matter) in float64, C-contiguous.
 
-Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
-(closed forms, hand-worked golden values, finite differences, invariants and
-an independent transcription of the pages' blocked loop).
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py``,
+``tests/test_oracle_window_pins.py`` and ``tests/test_oracle_blocks_pins.py``
+(closed forms, hand-worked golden values, finite differences, invariants,
+brute force on tiny inputs and an independent transcription of the pages'
+blocked loop).
 """
 from __future__ import annotations
 
@@ -84,6 +86,20 @@ def _load():
         lib.ora_attn_bwd_window.restype = None
         lib.ora_attn_bwd_window.argtypes = [dp, dp, dp, dp, i64, i64, i64, ctypes.c_double, i64,
                                             dp, dp, dp, dp, dp, dp]
+        u8 = ctypes.c_void_p
+        ci = ctypes.c_int
+        lib.ora_attn_probs_blocks.restype = None
+        lib.ora_attn_probs_blocks.argtypes = [dp, dp, dp, i64, i64, i64, ctypes.c_double, ci,
+                                              u8, i64, i64, dp]
+        lib.ora_attn_fwd_blocks.restype = None
+        lib.ora_attn_fwd_blocks.argtypes = [dp, dp, dp, i64, i64, i64, ctypes.c_double, ci,
+                                            u8, i64, i64, dp, dp]
+        lib.ora_attn_fwd_rows_blocks.restype = None
+        lib.ora_attn_fwd_rows_blocks.argtypes = [dp, dp, dp, i64, i64, i64, ctypes.c_double, ci,
+                                                 u8, i64, i64, lp, i64, dp, dp]
+        lib.ora_attn_bwd_blocks.restype = None
+        lib.ora_attn_bwd_blocks.argtypes = [dp, dp, dp, dp, i64, i64, i64, ctypes.c_double, ci,
+                                            u8, i64, i64, dp, dp, dp, dp, dp, dp]
         _lib = lib
         return lib
 
@@ -125,27 +141,59 @@ def _window(causal: bool, window):
     return int(window)
 
 
-def probs(q, k, v, tau: float, causal: bool, window=None) -> np.ndarray:
+def _blocks(blocks, BH: int, N: int, blk: int, window):
+    """blocks=None: no block mask.  Otherwise a block mask of blk x blk blocks,
+    shaped [nb, nb] (one mask for every head) or [BH, nb, nb] / [B, H, nb, nb]
+    (one per head), nb = ceil(N / blk); nonzero entries are visible blocks.
+    Returns (uint8 array, mask_heads) or None."""
+    if blocks is None:
+        return None
+    if window is not None:
+        raise ValueError("a block mask and a window do not combine")
+    if hasattr(blocks, "detach"):
+        blocks = blocks.detach().to("cpu").numpy()
+    m = np.ascontiguousarray(np.asarray(blocks) != 0, dtype=np.uint8)
+    blk = int(blk)
+    if blk < 1:
+        raise ValueError("blk must be >= 1")
+    nb = (N + blk - 1) // blk
+    if m.shape[-2:] != (nb, nb):
+        raise ValueError(f"block mask must end in ({nb}, {nb}), got {m.shape}")
+    heads = int(np.prod(m.shape[:-2])) if m.ndim > 2 else 1
+    if m.ndim > 2 and heads != BH:
+        raise ValueError(f"block mask has {heads} heads, expected 1 or {BH}")
+    return m, (1 if m.ndim == 2 else BH)
+
+
+def probs(q, k, v, tau: float, causal: bool, window=None, blocks=None, blk: int = 128) -> np.ndarray:
     """Attention probabilities P, shape [..., N, N]."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     BH, N, d = _dims(q)
     P = np.empty(q.shape[:-1] + (N,), dtype=np.float64)
     w = _window(causal, window)
-    if w is None:
+    bm = _blocks(blocks, BH, N, blk, window)
+    if bm is not None:
+        _load().ora_attn_probs_blocks(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), int(causal),
+                                      bm[0].ctypes.data, int(blk), bm[1], _ptr(P))
+    elif w is None:
         _load().ora_attn_probs(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), int(causal), _ptr(P))
     else:
         _load().ora_attn_probs_window(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), w, _ptr(P))
     return P
 
 
-def fwd(q, k, v, tau: float, causal: bool, window=None):
+def fwd(q, k, v, tau: float, causal: bool, window=None, blocks=None, blk: int = 128):
     """Full forward: returns (O [..., N, d], LSE [..., N])."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     BH, N, d = _dims(q)
     O = np.empty_like(q)
     L = np.empty(q.shape[:-1], dtype=np.float64)
     w = _window(causal, window)
-    if w is None:
+    bm = _blocks(blocks, BH, N, blk, window)
+    if bm is not None:
+        _load().ora_attn_fwd_blocks(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), int(causal),
+                                    bm[0].ctypes.data, int(blk), bm[1], _ptr(O), _ptr(L))
+    elif w is None:
         _load().ora_attn_fwd(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), int(causal),
                              _ptr(O), _ptr(L))
     else:
@@ -154,7 +202,7 @@ def fwd(q, k, v, tau: float, causal: bool, window=None):
     return O, L
 
 
-def fwd_rows(q, k, v, tau: float, causal: bool, rows, window=None):
+def fwd_rows(q, k, v, tau: float, causal: bool, rows, window=None, blocks=None, blk: int = 128):
     """Forward on selected rows.
 
     ``rows`` holds flat row ids ``bh * N + i``.  Returns (O_rows [n, d],
@@ -169,7 +217,12 @@ def fwd_rows(q, k, v, tau: float, causal: bool, rows, window=None):
     L = np.empty((r.size,), dtype=np.float64)
     rp = r.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
     w = _window(causal, window)
-    if w is None:
+    bm = _blocks(blocks, BH, N, blk, window)
+    if bm is not None:
+        _load().ora_attn_fwd_rows_blocks(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau),
+                                         int(causal), bm[0].ctypes.data, int(blk), bm[1],
+                                         rp, r.size, _ptr(O), _ptr(L))
+    elif w is None:
         _load().ora_attn_fwd_rows(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), int(causal),
                                   rp, r.size, _ptr(O), _ptr(L))
     else:
@@ -178,7 +231,8 @@ def fwd_rows(q, k, v, tau: float, causal: bool, rows, window=None):
     return O, L
 
 
-def bwd(q, k, v, do, tau: float, causal: bool, want_fwd: bool = False, window=None):
+def bwd(q, k, v, do, tau: float, causal: bool, want_fwd: bool = False, window=None,
+        blocks=None, blk: int = 128):
     """Analytic backward.  Returns (dQ, dK, dV) or, with ``want_fwd``,
     (dQ, dK, dV, O, LSE, D) where D is the softmax-Jacobian row sum."""
     q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
@@ -193,7 +247,12 @@ def bwd(q, k, v, do, tau: float, causal: bool, want_fwd: bool = False, window=No
     else:
         po = pl = pd = null
     w = _window(causal, window)
-    if w is None:
+    bm = _blocks(blocks, BH, N, blk, window)
+    if bm is not None:
+        _load().ora_attn_bwd_blocks(_ptr(q), _ptr(k), _ptr(v), _ptr(do), BH, N, d, float(tau),
+                                    int(causal), bm[0].ctypes.data, int(blk), bm[1],
+                                    _ptr(dQ), _ptr(dK), _ptr(dV), po, pl, pd)
+    elif w is None:
         _load().ora_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), BH, N, d, float(tau),
                              int(causal), _ptr(dQ), _ptr(dK), _ptr(dV), po, pl, pd)
     else:

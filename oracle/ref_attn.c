@@ -34,6 +34,14 @@
  *     layers attend within a window of the most recent tokens): key j is
  *     visible from query i iff i - w < j <= i, so w counts the query's own key;
  *     w >= N is plain causal attention;
+ *   - block-sparse attention ("FlashAttention e o gargalo real de
+ *     inferencia", section "o que isso custou": the block-sparse variant is an
+ *     approximation that skips blocks; "Atencao eficiente - FlashAttention,
+ *     sparse e hibrida", section "Sparse e hibrida": each token attends to a
+ *     subset, a local window plus global anchor tokens): a mask of blk x blk
+ *     blocks; key j is visible from query i only if mask[i / blk][j / blk] is
+ *     nonzero (and j <= i when causal).  A row that sees no key is an empty
+ *     sum: O_i = 0, LSE_i = -inf, and it contributes nothing to any gradient;
  *   - LSE is in natural-log units of the tau-scaled scores;
  *   - the backward is the analytic gradient of O with respect to Q, K, V for
  *     an upstream gradient dO, with the softmax Jacobian written out as
@@ -54,10 +62,24 @@
 #include <omp.h>
 #endif
 
-/* Key j is visible from query i (window > 0: only the `window` most recent keys). */
-static int visible(int64_t i, int64_t j, int causal, int64_t window)
+/* Which keys each query sees. */
+typedef struct {
+    int causal;            /* only keys j <= i */
+    int64_t window;        /* > 0: only the `window` most recent keys, i - window < j */
+    const uint8_t* blocks; /* NULL, or block masks [heads][nqb][nkb] (nonzero = visible) */
+    int64_t blk;           /* edge of a mask block, in rows and in keys */
+    int64_t nkb;           /* key blocks per mask row */
+    int64_t head_stride;   /* bytes from one head's mask to the next (0: shared mask) */
+} Visibility;
+
+/* Key j is visible from query i of head bh. */
+static int visible(const Visibility* vs, int64_t bh, int64_t i, int64_t j)
 {
-    return (!causal || j <= i) && (window <= 0 || j > i - window);
+    if (vs->causal && j > i) return 0;
+    if (vs->window > 0 && j <= i - vs->window) return 0;
+    if (vs->blocks && !vs->blocks[bh * vs->head_stride + (i / vs->blk) * vs->nkb + j / vs->blk])
+        return 0;
+    return 1;
 }
 
 static double dot(const double* a, const double* b, int64_t d)
@@ -71,25 +93,34 @@ static double dot(const double* a, const double* b, int64_t d)
  * One query row of the forward pass.
  *   q     : the query row (d values)
  *   K, V  : the keys and values of this head ([N][d])
- *   i     : the query's position (for the causal mask)
+ *   vs,bh,i: which keys query i of head bh sees
  *   p     : scratch of N doubles; on return p[j] = P_ij (0 for hidden keys)
  *   o     : d outputs, O_i = sum_j P_ij V_j
  *   lse   : m + ln l
+ * A query that sees no key gets p = 0, o = 0 and lse = -inf (the empty sum).
  */
 static void row_forward(const double* q, const double* K, const double* V,
-                        int64_t i, int64_t N, int64_t d, double tau, int causal, int64_t window,
-                        double* p, double* o, double* lse)
+                        const Visibility* vs, int64_t bh, int64_t i, int64_t N, int64_t d,
+                        double tau, double* p, double* o, double* lse)
 {
     double m = -INFINITY;
+    int64_t seen = 0;
     for (int64_t j = 0; j < N; ++j) {
-        if (visible(i, j, causal, window)) {
+        if (visible(vs, bh, i, j)) {
             p[j] = tau * dot(q, K + j * d, d);
             if (p[j] > m) m = p[j];
+            ++seen;
         }
+    }
+    if (seen == 0) {
+        for (int64_t j = 0; j < N; ++j) p[j] = 0.0;
+        for (int64_t k = 0; k < d; ++k) o[k] = 0.0;
+        *lse = -INFINITY;
+        return;
     }
     double l = 0.0;
     for (int64_t j = 0; j < N; ++j) {
-        if (visible(i, j, causal, window)) {
+        if (visible(vs, bh, i, j)) {
             p[j] = exp(p[j] - m);
             l += p[j];
         } else {
@@ -130,8 +161,8 @@ void ora_set_num_threads(int n)
  * visible scaled scores of query i; hidden keys get 0).  For small checks.
  */
 static void attn_probs(const double* Q, const double* K, const double* V,
-                       int64_t BH, int64_t N, int64_t d, double tau, int causal,
-                       int64_t window, double* P)
+                       int64_t BH, int64_t N, int64_t d, double tau, const Visibility* vs,
+                       double* P)
 {
     int64_t rows = BH * N;
 #pragma omp parallel
@@ -141,8 +172,8 @@ static void attn_probs(const double* Q, const double* K, const double* V,
         for (int64_t r = 0; r < rows; ++r) {
             int64_t bh = r / N, i = r % N;
             double lse;
-            row_forward(Q + r * d, K + bh * N * d, V + bh * N * d, i, N, d, tau,
-                        causal, window, P + r * N, o, &lse);
+            row_forward(Q + r * d, K + bh * N * d, V + bh * N * d, vs, bh, i, N, d, tau,
+                        P + r * N, o, &lse);
         }
         free(o);
     }
@@ -150,8 +181,8 @@ static void attn_probs(const double* Q, const double* K, const double* V,
 
 /* Forward pass over every row: O [BH][N][d], LSE [BH][N]. */
 static void attn_fwd(const double* Q, const double* K, const double* V,
-                     int64_t BH, int64_t N, int64_t d, double tau, int causal,
-                     int64_t window, double* O, double* LSE)
+                     int64_t BH, int64_t N, int64_t d, double tau, const Visibility* vs,
+                     double* O, double* LSE)
 {
     int64_t rows = BH * N;
 #pragma omp parallel
@@ -160,8 +191,8 @@ static void attn_fwd(const double* Q, const double* K, const double* V,
 #pragma omp for schedule(dynamic, 16)
         for (int64_t r = 0; r < rows; ++r) {
             int64_t bh = r / N, i = r % N;
-            row_forward(Q + r * d, K + bh * N * d, V + bh * N * d, i, N, d, tau,
-                        causal, window, p, O + r * d, LSE + r);
+            row_forward(Q + r * d, K + bh * N * d, V + bh * N * d, vs, bh, i, N, d, tau,
+                        p, O + r * d, LSE + r);
         }
         free(p);
     }
@@ -172,8 +203,8 @@ static void attn_fwd(const double* Q, const double* K, const double* V,
  * head bh; outputs O_rows [nrows][d] and LSE_rows [nrows] in the same order.
  */
 static void attn_fwd_rows(const double* Q, const double* K, const double* V,
-                          int64_t BH, int64_t N, int64_t d, double tau, int causal,
-                          int64_t window, const int64_t* rows, int64_t nrows,
+                          int64_t BH, int64_t N, int64_t d, double tau, const Visibility* vs,
+                          const int64_t* rows, int64_t nrows,
                           double* O_rows, double* LSE_rows)
 {
     (void)BH;
@@ -184,8 +215,8 @@ static void attn_fwd_rows(const double* Q, const double* K, const double* V,
         for (int64_t k = 0; k < nrows; ++k) {
             int64_t r = rows[k];
             int64_t bh = r / N, i = r % N;
-            row_forward(Q + r * d, K + bh * N * d, V + bh * N * d, i, N, d, tau,
-                        causal, window, p, O_rows + k * d, LSE_rows + k);
+            row_forward(Q + r * d, K + bh * N * d, V + bh * N * d, vs, bh, i, N, d, tau,
+                        p, O_rows + k * d, LSE_rows + k);
         }
         free(p);
     }
@@ -208,7 +239,7 @@ static void attn_fwd_rows(const double* Q, const double* K, const double* V,
  */
 static void attn_bwd(const double* Q, const double* K, const double* V,
                      const double* dO,
-                     int64_t BH, int64_t N, int64_t d, double tau, int causal, int64_t window,
+                     int64_t BH, int64_t N, int64_t d, double tau, const Visibility* vs,
                      double* dQ, double* dK, double* dV,
                      double* O_out, double* LSE_out, double* D_out)
 {
@@ -230,8 +261,7 @@ static void attn_bwd(const double* Q, const double* K, const double* V,
             /* forward: P and (optionally) O, LSE */
             for (int64_t i = 0; i < N; ++i) {
                 double lse;
-                row_forward(Qh + i * d, Kh, Vh, i, N, d, tau, causal, window,
-                            P + i * N, o, &lse);
+                row_forward(Qh + i * d, Kh, Vh, vs, bh, i, N, d, tau, P + i * N, o, &lse);
                 if (O_out) memcpy(O_out + (bh * N + i) * d, o, sizeof(double) * (size_t)d);
                 if (LSE_out) LSE_out[bh * N + i] = lse;
             }
@@ -241,7 +271,7 @@ static void attn_bwd(const double* Q, const double* K, const double* V,
                 const double* Pi = P + i * N;
                 double Di = 0.0;
                 for (int64_t j = 0; j < N; ++j) {
-                    dSi[j] = visible(i, j, causal, window) ? dot(dOh + i * d, Vh + j * d, d) : 0.0;
+                    dSi[j] = visible(vs, bh, i, j) ? dot(dOh + i * d, Vh + j * d, d) : 0.0;
                     Di += Pi[j] * dSi[j];
                 }
                 for (int64_t j = 0; j < N; ++j) dSi[j] = Pi[j] * (dSi[j] - Di);
@@ -280,51 +310,74 @@ static void attn_bwd(const double* Q, const double* K, const double* V,
 }
 
 /* ---------------------------------------------------------------- exports --
- * Plain entry points (no window) and sliding-window entry points (causal,
- * key j visible from query i iff i - window < j <= i, window >= 1). */
+ * Plain entry points (no window), sliding-window entry points (causal, key j
+ * visible from query i iff i - window < j <= i, window >= 1) and block-mask
+ * entry points (blocks: [mask_heads][nqb][nkb] bytes with nqb = nkb =
+ * ceil(N / blk), mask_heads 1 = one mask for every head, else BH). */
+static Visibility plain_vis(int causal, int64_t window)
+{
+    Visibility vs = {causal, window, NULL, 1, 0, 0};
+    return vs;
+}
+
+static Visibility block_vis(int causal, const uint8_t* blocks, int64_t blk, int64_t mask_heads,
+                            int64_t N)
+{
+    int64_t nb = (N + blk - 1) / blk;
+    Visibility vs = {causal, 0, blocks, blk, nb, mask_heads == 1 ? 0 : nb * nb};
+    return vs;
+}
+
 void ora_attn_probs(const double* Q, const double* K, const double* V, int64_t BH, int64_t N,
                     int64_t d, double tau, int causal, double* P)
 {
-    attn_probs(Q, K, V, BH, N, d, tau, causal, 0, P);
+    Visibility vs = plain_vis(causal, 0);
+    attn_probs(Q, K, V, BH, N, d, tau, &vs, P);
 }
 
 void ora_attn_fwd(const double* Q, const double* K, const double* V, int64_t BH, int64_t N,
                   int64_t d, double tau, int causal, double* O, double* LSE)
 {
-    attn_fwd(Q, K, V, BH, N, d, tau, causal, 0, O, LSE);
+    Visibility vs = plain_vis(causal, 0);
+    attn_fwd(Q, K, V, BH, N, d, tau, &vs, O, LSE);
 }
 
 void ora_attn_fwd_rows(const double* Q, const double* K, const double* V, int64_t BH, int64_t N,
                        int64_t d, double tau, int causal, const int64_t* rows, int64_t nrows,
                        double* O_rows, double* LSE_rows)
 {
-    attn_fwd_rows(Q, K, V, BH, N, d, tau, causal, 0, rows, nrows, O_rows, LSE_rows);
+    Visibility vs = plain_vis(causal, 0);
+    attn_fwd_rows(Q, K, V, BH, N, d, tau, &vs, rows, nrows, O_rows, LSE_rows);
 }
 
 void ora_attn_bwd(const double* Q, const double* K, const double* V, const double* dO,
                   int64_t BH, int64_t N, int64_t d, double tau, int causal,
                   double* dQ, double* dK, double* dV, double* O_out, double* LSE_out, double* D_out)
 {
-    attn_bwd(Q, K, V, dO, BH, N, d, tau, causal, 0, dQ, dK, dV, O_out, LSE_out, D_out);
+    Visibility vs = plain_vis(causal, 0);
+    attn_bwd(Q, K, V, dO, BH, N, d, tau, &vs, dQ, dK, dV, O_out, LSE_out, D_out);
 }
 
 void ora_attn_probs_window(const double* Q, const double* K, const double* V, int64_t BH,
                            int64_t N, int64_t d, double tau, int64_t window, double* P)
 {
-    attn_probs(Q, K, V, BH, N, d, tau, 1, window, P);
+    Visibility vs = plain_vis(1, window);
+    attn_probs(Q, K, V, BH, N, d, tau, &vs, P);
 }
 
 void ora_attn_fwd_window(const double* Q, const double* K, const double* V, int64_t BH, int64_t N,
                          int64_t d, double tau, int64_t window, double* O, double* LSE)
 {
-    attn_fwd(Q, K, V, BH, N, d, tau, 1, window, O, LSE);
+    Visibility vs = plain_vis(1, window);
+    attn_fwd(Q, K, V, BH, N, d, tau, &vs, O, LSE);
 }
 
 void ora_attn_fwd_rows_window(const double* Q, const double* K, const double* V, int64_t BH,
                               int64_t N, int64_t d, double tau, int64_t window,
                               const int64_t* rows, int64_t nrows, double* O_rows, double* LSE_rows)
 {
-    attn_fwd_rows(Q, K, V, BH, N, d, tau, 1, window, rows, nrows, O_rows, LSE_rows);
+    Visibility vs = plain_vis(1, window);
+    attn_fwd_rows(Q, K, V, BH, N, d, tau, &vs, rows, nrows, O_rows, LSE_rows);
 }
 
 void ora_attn_bwd_window(const double* Q, const double* K, const double* V, const double* dO,
@@ -332,5 +385,41 @@ void ora_attn_bwd_window(const double* Q, const double* K, const double* V, cons
                          double* dQ, double* dK, double* dV, double* O_out, double* LSE_out,
                          double* D_out)
 {
-    attn_bwd(Q, K, V, dO, BH, N, d, tau, 1, window, dQ, dK, dV, O_out, LSE_out, D_out);
+    Visibility vs = plain_vis(1, window);
+    attn_bwd(Q, K, V, dO, BH, N, d, tau, &vs, dQ, dK, dV, O_out, LSE_out, D_out);
+}
+
+void ora_attn_probs_blocks(const double* Q, const double* K, const double* V, int64_t BH,
+                           int64_t N, int64_t d, double tau, int causal, const uint8_t* blocks,
+                           int64_t blk, int64_t mask_heads, double* P)
+{
+    Visibility vs = block_vis(causal, blocks, blk, mask_heads, N);
+    attn_probs(Q, K, V, BH, N, d, tau, &vs, P);
+}
+
+void ora_attn_fwd_blocks(const double* Q, const double* K, const double* V, int64_t BH, int64_t N,
+                         int64_t d, double tau, int causal, const uint8_t* blocks, int64_t blk,
+                         int64_t mask_heads, double* O, double* LSE)
+{
+    Visibility vs = block_vis(causal, blocks, blk, mask_heads, N);
+    attn_fwd(Q, K, V, BH, N, d, tau, &vs, O, LSE);
+}
+
+void ora_attn_fwd_rows_blocks(const double* Q, const double* K, const double* V, int64_t BH,
+                              int64_t N, int64_t d, double tau, int causal, const uint8_t* blocks,
+                              int64_t blk, int64_t mask_heads, const int64_t* rows, int64_t nrows,
+                              double* O_rows, double* LSE_rows)
+{
+    Visibility vs = block_vis(causal, blocks, blk, mask_heads, N);
+    attn_fwd_rows(Q, K, V, BH, N, d, tau, &vs, rows, nrows, O_rows, LSE_rows);
+}
+
+void ora_attn_bwd_blocks(const double* Q, const double* K, const double* V, const double* dO,
+                         int64_t BH, int64_t N, int64_t d, double tau, int causal,
+                         const uint8_t* blocks, int64_t blk, int64_t mask_heads,
+                         double* dQ, double* dK, double* dV, double* O_out, double* LSE_out,
+                         double* D_out)
+{
+    Visibility vs = block_vis(causal, blocks, blk, mask_heads, N);
+    attn_bwd(Q, K, V, dO, BH, N, d, tau, &vs, dQ, dK, dV, O_out, LSE_out, D_out);
 }

@@ -13,14 +13,22 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "ref_attn.c")
-PIN_FILES = [os.path.join(ROOT, "tests", f) for f in ("test_oracle_pins.py", "test_oracle_window_pins.py")]
+PIN_FILES = [os.path.join(ROOT, "tests", f)
+             for f in ("test_oracle_pins.py", "test_oracle_window_pins.py", "test_oracle_blocks_pins.py")]
 
 MUTANTS = {
     "scores_without_tau": ("p[j] = tau * dot(q, K + j * d, d);", "p[j] = dot(q, K + j * d, d);"),
-    "causal_mask_reversed": ("(!causal || j <= i)", "(!causal || j >= i)"),
-    "causal_mask_strict": ("(!causal || j <= i)", "(!causal || j < i || i == 0)"),
-    "window_off_by_one": ("(window <= 0 || j > i - window)", "(window <= 0 || j >= i - window)"),
-    "window_ignored": ("(window <= 0 || j > i - window)", "(window <= 0 || j > i - 2 * window)"),
+    "causal_mask_reversed": ("if (vs->causal && j > i) return 0;", "if (vs->causal && j < i) return 0;"),
+    "causal_mask_strict": ("if (vs->causal && j > i) return 0;", "if (vs->causal && j >= i && i > 0) return 0;"),
+    "window_off_by_one": ("if (vs->window > 0 && j <= i - vs->window) return 0;",
+                          "if (vs->window > 0 && j < i - vs->window) return 0;"),
+    "window_ignored": ("if (vs->window > 0 && j <= i - vs->window) return 0;",
+                       "if (vs->window > 0 && j <= i - 2 * vs->window) return 0;"),
+    "blocks_transposed": ("(i / vs->blk) * vs->nkb + j / vs->blk]", "(j / vs->blk) * vs->nkb + i / vs->blk]"),
+    "blocks_ignored": ("if (vs->blocks && !vs->blocks[", "if (0 && !vs->blocks["),
+    "blocks_one_head": ("vs->blocks[bh * vs->head_stride + ", "vs->blocks[0 * vs->head_stride + "),
+    "blocks_edge_off_by_one": ("(i / vs->blk) * vs->nkb + j / vs->blk]", "((i + 1) / vs->blk) * vs->nkb + j / vs->blk]"),
+    "empty_row_not_guarded": ("    if (seen == 0) {", "    if (seen < 0) {"),
     "lse_without_max": ("*lse = m + log(l);", "*lse = log(l);"),
     "no_normalisation": ("for (int64_t j = 0; j < N; ++j) p[j] /= l;", ""),
     "output_wrong_value_row": ("const double* v = V + j * d;", "const double* v = V + (N - 1 - j) * d;"),
