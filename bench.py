@@ -301,6 +301,8 @@ def run_ours(args):
 
     window_leg = (measure_window(w, q, k, v, do, dev, args.window, min(args.steps, 20), peak)
                   if args.window > 0 and w.causal else None)
+    blocks_leg = (measure_blocks(w, q, k, v, do, dev, min(args.steps, 20), peak)
+                  if args.blocks and w.causal else None)
     e2e = run_e2e(args, w, x, dev, f_step) if not args.no_e2e else None
     cpu = run_cpu_baseline(w, budget_s=args.cpu_seconds) if (rank == 0 and not args.no_cpu) else None
 
@@ -327,6 +329,7 @@ def run_ours(args):
         "fwd_bwd_step": {"ms": round(step_avg_ms, 4), "tflops_per_gpu": round(value / world, 2)},
         "roofline": roofline,
         "sliding_window": window_leg,
+        "block_sparse": blocks_leg,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 4 * args.steps,
@@ -347,10 +350,26 @@ def window_flops_fwd(B, H, N, d, window):
     return 4.0 * B * H * d * visible
 
 
-def measure_window(w, q, k, v, do, dev, window, steps, peak):
-    """The same workload with a causal sliding window (fa_fwd_window /
-    fa_bwd_window): per-kernel CUDA-event times and TFLOP/s on the window's
-    counted FLOPs (backward = 2.5 x forward)."""
+def blocks_flops_fwd(B, H, N, d, causal, mask):
+    """Counted forward FLOPs with a block mask: 4 d per visible score.  Block
+    (i, j) holds rows_i x keys_j scores; with causal, the diagonal block holds
+    rows_i (rows_i + 1) / 2 and blocks above it none.  mask: [nb, nb] (one for
+    every head) or [B*H, nb, nb]."""
+    import numpy as np
+    nb = mask.shape[-1]
+    sizes = np.minimum(128, N - 128 * np.arange(nb)).astype(np.float64)
+    cnt = np.outer(sizes, sizes)
+    if causal:
+        cnt = np.tril(cnt, -1) + np.diag(sizes * (sizes + 1) / 2)
+    m = (np.asarray(mask) != 0).reshape(-1, nb, nb)
+    visible = float((m * cnt).sum()) * (B * H if m.shape[0] == 1 else 1)
+    return 4.0 * d * visible
+
+
+def measure_variant(w, q, k, v, do, dev, steps, peak, ff, **mask):
+    """The same workload with a mask variant (window=... or blocks=..., passed
+    to api.fwd / api.bwd): per-kernel CUDA-event times and TFLOP/s on the
+    variant's counted forward FLOPs ff (backward = 2.5 x forward)."""
     import torch
     from exact_io_aware_12_gb300 import api, _lib
 
@@ -362,8 +381,8 @@ def measure_window(w, q, k, v, do, dev, window, steps, peak):
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     for _ in range(3):
-        api.fwd(q, k, v, True, w.tau, out=o, lse=lse, window=window)
-        api.bwd(q, k, v, o, do, lse, True, w.tau, dq=dq, dk=dk, dv=dv, workspace=ws, window=window)
+        api.fwd(q, k, v, True, w.tau, out=o, lse=lse, **mask)
+        api.bwd(q, k, v, o, do, lse, True, w.tau, dq=dq, dk=dk, dv=dv, workspace=ws, **mask)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
     for e in sum(ev, []):
         e.record(stream)
@@ -371,22 +390,46 @@ def measure_window(w, q, k, v, do, dev, window, steps, peak):
     for i in range(steps):
         flush.fill_(float(i))
         _lib.check(_lib.fa_set_timing_events(ev[i][0].cuda_event, ev[i][1].cuda_event), "timing")
-        api.fwd(q, k, v, True, w.tau, out=o, lse=lse, window=window)
+        api.fwd(q, k, v, True, w.tau, out=o, lse=lse, **mask)
         _lib.check(_lib.fa_set_timing_events(ev[i][2].cuda_event, ev[i][3].cuda_event), "timing")
-        api.bwd(q, k, v, o, do, lse, True, w.tau, dq=dq, dk=dk, dv=dv, workspace=ws, window=window)
+        api.bwd(q, k, v, o, do, lse, True, w.tau, dq=dq, dk=dk, dv=dv, workspace=ws, **mask)
         _lib.check(_lib.fa_set_timing_events(None, None), "timing")
     torch.cuda.synchronize(dev)
     if api.last_device_error(dev) != _lib.FA_OK:
-        raise RuntimeError("kernel watchdog fired in the sliding-window leg")
+        raise RuntimeError(f"kernel watchdog fired in the {sorted(mask)} leg")
     fms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
     bms = sum(e[2].elapsed_time(e[3]) for e in ev) / steps
-    ff = window_flops_fwd(B, H, N, d, window)
-    return {"window": window, "steps": steps,
+    return {"steps": steps,
             "fwd": {"ms": round(fms, 4), "tflops": round(ff / fms / 1e9, 2),
                     "frac": round(ff / fms / 1e9 / peak, 4)},
             "bwd_main_kernel": {"ms": round(bms, 4), "tflops": round(2.5 * ff / bms / 1e9, 2),
                                 "frac": round(2.5 * ff / bms / 1e9 / peak, 4)},
             "flops_fwd": ff}
+
+
+def measure_window(w, q, k, v, do, dev, window, steps, peak):
+    """Causal sliding window of `window` keys (fa_fwd_window / fa_bwd_window)."""
+    B, H, N, d = w.shape
+    ff = window_flops_fwd(B, H, N, d, window)
+    return {"window": window, **measure_variant(w, q, k, v, do, dev, steps, peak, ff, window=window)}
+
+
+def measure_blocks(w, q, k, v, do, dev, steps, peak):
+    """Block-sparse causal attention (fa_fwd_blocks / fa_bwd_blocks) with a
+    seeded per-head local + global-anchor mask: 4 local blocks (512 tokens),
+    2 anchor blocks (256 tokens), 2% random extra blocks."""
+    import torch
+    from exact_io_aware_12_gb300.workloads import local_global_block_mask
+
+    B, H, N, d = w.shape
+    nb = (N + 127) // 128
+    m = local_global_block_mask(nb, local=4, anchors=2, heads=B * H, extra=0.02, seed=3)
+    ff = blocks_flops_fwd(B, H, N, d, True, m)
+    dense = 4.0 * B * H * N * N * d / 2
+    mt = torch.from_numpy(m).to(dev).reshape(B, H, nb, nb)
+    return {"mask": "per head: 4 local + 2 anchor blocks of 128, 2% random extra (seed 3)",
+            "causal_work_fraction": round(ff / dense, 4),
+            **measure_variant(w, q, k, v, do, dev, steps, peak, ff, blocks=mt)}
 
 
 def run_e2e(args, w, x, dev, f_step):
@@ -524,6 +567,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--window", type=int, default=4096,
                     help="also time the causal sliding-window kernels with this window (0: skip)")
+    ap.add_argument("--no-blocks", dest="blocks", action="store_false",
+                    help="skip the block-sparse leg")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -37,7 +37,14 @@ SIGNATURES = {
     "fa_fwd_window": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_window": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_fwd_blocks": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _I, _P]),
+    "fa_bwd_blocks": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _F, _I,
+                           _P, _I, _P]),
 }
+
+# Block-mask geometry (FA_BLOCK_MASK_EDGE, FA_BLOCK_MASK_MAX_N).
+BLOCK_MASK_EDGE = 128
+BLOCK_MASK_MAX_N = 131072
 
 # Size of the fixed scratch array fa_bwd_noalloc uses (FA_NOALLOC_SCRATCH_BYTES).
 NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -95,6 +102,17 @@ def fa_bwd_window(Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B
                   window, stream) -> int:
     return _call("fa_bwd_window", Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B,
                  H, N, d, tau, window, stream)
+
+
+def fa_fwd_blocks(Q, K, V, O, LSE, B, H, N, d, tau, causal, block_mask, mask_heads, stream) -> int:
+    return _call("fa_fwd_blocks", Q, K, V, O, LSE, B, H, N, d, tau, causal, block_mask, mask_heads,
+                 stream)
+
+
+def fa_bwd_blocks(Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, tau,
+                  causal, block_mask, mask_heads, stream) -> int:
+    return _call("fa_bwd_blocks", Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B,
+                 H, N, d, tau, causal, block_mask, mask_heads, stream)
 
 
 def fa_bwd_workspace_size(B, H, N, d) -> int:

@@ -31,14 +31,38 @@ def _check_inputs(*ts: torch.Tensor) -> Tuple[int, int, int, int]:
     return B, H, N, d
 
 
+def _check_blocks(blocks: torch.Tensor, ref: torch.Tensor) -> int:
+    """A block mask: CUDA uint8/bool, contiguous, shaped [nb, nb] (one mask) or
+    [B, H, nb, nb] / [B*H, nb, nb] (one per head), nb = ceil(N / 128).
+    Returns mask_heads."""
+    B, H, N, _ = ref.shape
+    nb = (N + _lib.BLOCK_MASK_EDGE - 1) // _lib.BLOCK_MASK_EDGE
+    if not blocks.is_cuda or blocks.device != ref.device or not blocks.is_contiguous():
+        raise ValueError("block mask must be a contiguous tensor on the inputs' device")
+    if blocks.dtype not in (torch.uint8, torch.bool):
+        raise ValueError("block mask must be uint8 or bool")
+    if tuple(blocks.shape[-2:]) != (nb, nb):
+        raise ValueError(f"block mask must end in ({nb}, {nb})")
+    heads = blocks.numel() // (nb * nb)
+    if blocks.dim() == 2:
+        return 1
+    if heads != B * H:
+        raise ValueError(f"block mask has {heads} heads, expected 1 or {B * H}")
+    return heads
+
+
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool,
         tau: Optional[float] = None, out: Optional[torch.Tensor] = None,
-        lse: Optional[torch.Tensor] = None, o_fp32: bool = False, window: Optional[int] = None):
+        lse: Optional[torch.Tensor] = None, o_fp32: bool = False, window: Optional[int] = None,
+        blocks: Optional[torch.Tensor] = None):
     """Forward pass.  Returns (O, LSE): O bf16 (fp32 with ``o_fp32``) and LSE
     fp32 [B, H, N].  ``window`` (with ``causal``): each query sees only its
-    ``window`` most recent keys (fa_fwd_window)."""
+    ``window`` most recent keys (fa_fwd_window).  ``blocks``: a block mask
+    over 128 x 128 blocks (fa_fwd_blocks)."""
     if window is not None and (not causal or o_fp32):
         raise ValueError("a window needs causal=True and a bf16 O")
+    if blocks is not None and (o_fp32 or window is not None):
+        raise ValueError("a block mask needs a bf16 O and no window")
     B, H, N, d = _check_inputs(q, k, v)
     tau = 1.0 / math.sqrt(d) if tau is None else float(tau)
     o_dtype = torch.float32 if o_fp32 else torch.bfloat16
@@ -46,6 +70,13 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool,
         out = torch.empty(q.shape, dtype=o_dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if blocks is not None:
+        heads = _check_blocks(blocks, q)
+        code = _lib.fa_fwd_blocks(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  lse.data_ptr(), B, H, N, d, tau, int(bool(causal)),
+                                  blocks.data_ptr(), heads, _stream_handle(q.device))
+        _lib.check(code, "fa_fwd_blocks")
+        return out, lse
     if window is not None:
         code = _lib.fa_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                   lse.data_ptr(), B, H, N, d, tau, int(window),
@@ -66,7 +97,7 @@ def workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 def bwd(q, k, v, o, do, lse, causal: bool, tau: Optional[float] = None,
         dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None,
         dv: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-        window: Optional[int] = None):
+        window: Optional[int] = None, blocks: Optional[torch.Tensor] = None):
     """Backward pass.  Returns (dQ, dK, dV), bf16.  ``workspace`` (a byte
     tensor of at least ``workspace_bytes`` bytes) is allocated with torch when
     not given, so the library itself allocates nothing."""
@@ -80,6 +111,17 @@ def bwd(q, k, v, o, do, lse, causal: bool, tau: Optional[float] = None,
     need = workspace_bytes(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if blocks is not None:
+        if window is not None:
+            raise ValueError("a block mask needs no window")
+        heads = _check_blocks(blocks, q)
+        code = _lib.fa_bwd_blocks(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                  dv.data_ptr(), workspace.data_ptr(), workspace.numel(), B, H, N,
+                                  d, tau, int(bool(causal)), blocks.data_ptr(), heads,
+                                  _stream_handle(q.device))
+        _lib.check(code, "fa_bwd_blocks")
+        return dq, dk, dv
     if window is not None:
         if not causal:
             raise ValueError("a window needs causal=True")

@@ -108,11 +108,32 @@ fa_status check_shape(int B, int H, int N, int d, float tau, int causal, bool* e
 
 fa_status map_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
+// Block-mask checks: mask_heads is 1 or B*H and the mask fits the kernels'
+// per-tile bit sets.  Sets *bytes (the mask's size) and *head_stride.
+fa_status check_blocks(const uint8_t* blocks, int mask_heads, int B, int H, int N, size_t* bytes,
+                       long long* head_stride) {
+    if (blocks == nullptr) return FA_ERR_INVALID_ARG;
+    const long long bh = static_cast<long long>(B) * H;
+    if (mask_heads != 1 && mask_heads != bh) return FA_ERR_INVALID_ARG;
+    const long long nb = (static_cast<long long>(N) + kMaskBlockEdge - 1) / kMaskBlockEdge;
+    if (nb > kMaxMaskBlocks) return FA_ERR_UNSUPPORTED;
+    *bytes = static_cast<size_t>(mask_heads) * static_cast<size_t>(nb * nb);
+    *head_stride = mask_heads == 1 ? 0 : nb * nb;
+    return FA_OK;
+}
+
 fa_status fwd_common(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
-                     int N, int d, float tau, int causal, void* stream, bool o32, int window = 0) {
+                     int N, int d, float tau, int causal, void* stream, bool o32, int window = 0,
+                     const uint8_t* blocks = nullptr, int mask_heads = 0) {
     bool empty = false;
     fa_status s = check_shape(B, H, N, d, tau, causal, &empty);
     if (s != FA_OK || empty) return s;
+    size_t mask_bytes = 0;
+    long long mask_stride = 0;
+    if (mask_heads != 0) {
+        s = check_blocks(blocks, mask_heads, B, H, N, &mask_bytes, &mask_stride);
+        if (s != FA_OK) return s;
+    }
     const void* ptrs[] = {Q, K, V, O, LSE};
     for (const void* p : ptrs)
         if (p == nullptr || !aligned16(p)) return FA_ERR_INVALID_ARG;
@@ -123,6 +144,8 @@ fa_status fwd_common(const void* Q, const void* K, const void* V, void* O, float
         if (overlaps(O, o_bytes, in, in_bytes) || overlaps(LSE, l_bytes, in, in_bytes))
             return FA_ERR_INVALID_ARG;
     if (overlaps(O, o_bytes, LSE, l_bytes)) return FA_ERR_INVALID_ARG;
+    if (blocks && (overlaps(O, o_bytes, blocks, mask_bytes) || overlaps(LSE, l_bytes, blocks, mask_bytes)))
+        return FA_ERR_INVALID_ARG;
     DeviceInfo* di = current_device(&s);
     if (!di) return s;
     FwdArgs a;
@@ -137,6 +160,8 @@ fa_status fwd_common(const void* Q, const void* K, const void* V, void* O, float
     a.tau = tau;
     a.causal = causal != 0;
     a.window = window;
+    a.blocks = blocks;
+    a.blocks_head_stride = mask_stride;
     a.o32 = o32;
     a.err = di->err_word;
     a.wait_limit_ns = g_wait_limit_ns.load();
@@ -210,10 +235,17 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 static fa_status bwd_common(const void* Q, const void* K, const void* V, const void* O,
                             const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
                             void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
-                            float tau, int causal, int window, void* stream) {
+                            float tau, int causal, int window, void* stream,
+                            const uint8_t* blocks = nullptr, int mask_heads = 0) {
     bool empty = false;
     fa_status s = check_shape(B, H, N, d, tau, causal, &empty);
     if (s != FA_OK || empty) return s;
+    size_t mask_bytes = 0;
+    long long mask_stride = 0;
+    if (mask_heads != 0) {
+        s = check_blocks(blocks, mask_heads, B, H, N, &mask_bytes, &mask_stride);
+        if (s != FA_OK) return s;
+    }
     const void* ptrs[] = {Q, K, V, O, dO, LSE, dQ, dK, dV};
     for (const void* p : ptrs)
         if (p == nullptr || !aligned16(p)) return FA_ERR_INVALID_ARG;
@@ -229,6 +261,9 @@ static fa_status bwd_common(const void* Q, const void* K, const void* V, const v
     }
     if (overlaps(dQ, tb, dK, tb) || overlaps(dQ, tb, dV, tb) || overlaps(dK, tb, dV, tb))
         return FA_ERR_INVALID_ARG;
+    if (blocks)
+        for (void* o : outs)
+            if (overlaps(o, tb, blocks, mask_bytes)) return FA_ERR_INVALID_ARG;
     const size_t need = fa_bwd_workspace_size(B, H, N, d);
     if (workspace != nullptr) {
         if (workspace_bytes < need) return FA_ERR_WORKSPACE;
@@ -236,6 +271,7 @@ static fa_status bwd_common(const void* Q, const void* K, const void* V, const v
         for (const void* p : all)
             if (overlaps(workspace, need, p, tb)) return FA_ERR_INVALID_ARG;
         if (overlaps(workspace, need, LSE, rows * 4)) return FA_ERR_INVALID_ARG;
+        if (blocks && overlaps(workspace, need, blocks, mask_bytes)) return FA_ERR_INVALID_ARG;
     }
     DeviceInfo* di = current_device(&s);
     if (!di) return s;
@@ -263,6 +299,8 @@ static fa_status bwd_common(const void* Q, const void* K, const void* V, const v
     a.tau = tau;
     a.causal = causal != 0;
     a.window = window;
+    a.blocks = blocks;
+    a.blocks_head_stride = mask_stride;
     a.err = di->err_word;
     a.wait_limit_ns = g_wait_limit_ns.load();
     a.ev_start = t_ev_start;
@@ -293,6 +331,23 @@ fa_status fa_bwd_window(const void* Q, const void* K, const void* V, const void*
     if (window < 1) return FA_ERR_INVALID_ARG;
     return bwd_common(Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, tau,
                       1, window, stream);
+}
+
+fa_status fa_fwd_blocks(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                        int H, int N, int d, float tau, int causal, const unsigned char* block_mask,
+                        int mask_heads, void* stream) {
+    if (mask_heads == 0) return FA_ERR_INVALID_ARG;
+    return fwd_common(Q, K, V, O, LSE, B, H, N, d, tau, causal, stream, false, 0, block_mask,
+                      mask_heads);
+}
+
+fa_status fa_bwd_blocks(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                        const float* LSE, void* dQ, void* dK, void* dV, void* workspace,
+                        size_t workspace_bytes, int B, int H, int N, int d, float tau, int causal,
+                        const unsigned char* block_mask, int mask_heads, void* stream) {
+    if (mask_heads == 0) return FA_ERR_INVALID_ARG;
+    return bwd_common(Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H, N, d, tau,
+                      causal, 0, stream, block_mask, mask_heads);
 }
 
 const char* fa_status_string(fa_status s) {

@@ -47,6 +47,9 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kReducerWarp = 10;
 constexpr float kLog2e = 1.44269504088896341f;
+// Which query tiles a key tile visits beyond causality.
+enum : int { kMaskNone = 0, kMaskWindow = 1, kMaskBlocks = 2 };
+constexpr int kMaskWords = kMaxMaskBlocks / 32;
 
 template <int D>
 struct BwdLayout {
@@ -81,6 +84,7 @@ struct BwdBarriers {
     uint64_t dq_staged;
     uint32_t tmem_base;
     int abort_flag;
+    uint32_t qbits[kMaskWords];  // kMaskBlocks: bit i = this key tile is visited by query tile i
 };
 
 struct BwdParams {
@@ -93,6 +97,8 @@ struct BwdParams {
     float tau;
     unsigned int* err;
     unsigned long long wait_limit_ns;
+    const uint8_t* blocks;          // block mask [heads][n_kv][n_kv] (kMaskBlocks)
+    long long blocks_head_stride;   // bytes between heads' masks (0: one mask)
 };
 
 enum : uint32_t {
@@ -145,8 +151,9 @@ __device__ __forceinline__ void mma_mn_mn(uint32_t tmem_d, uint32_t a_lo, uint32
         mma_ss_warp<1>(tmem_d, a_lo + ((k * 2048) >> 4), b_lo + ((k * 2048) >> 4), kDescHi, id);
 }
 
-// LOCAL: causal sliding window of p.window keys (only with CAUSAL).
-template <int D, bool CAUSAL, bool LOCAL>
+// MASK: kMaskNone; kMaskWindow, a causal sliding window of p.window keys (only
+// with CAUSAL); kMaskBlocks, the block mask p.blocks.
+template <int D, bool CAUSAL, int MASK>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -154,6 +161,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                    const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                    const BwdParams p) {
     using L = BwdLayout<D>;
+    static_assert(sizeof(BwdBarriers) <= L::kBytes - L::kBars, "barrier block overflows its slot");
+    constexpr bool LOCAL = MASK == kMaskWindow;
+    constexpr bool SPARSE = MASK == kMaskBlocks;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
     BwdBarriers& sh = *reinterpret_cast<BwdBarriers*>(smem + L::kBars);
@@ -172,7 +182,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const int window = (CAUSAL && LOCAL) ? p.window : 0;
     const int first = CAUSAL ? kv_tile : 0;
     const int last = window > 0 ? min(n_q - 1, (kv_start + kBK - 1 + window - 1) / kBQ) : n_q - 1;
-    const int n_steps = last - first + 1;
+    int n_steps = last - first + 1;  // with a block mask: counted below
 
     if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicCAS(p.err, 0u, 1u | (0xAAu << 8));
@@ -217,26 +227,54 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         tma_prefetch_map(&tmdO);
         tma_prefetch_map(&tmdQacc);
     }
+    if constexpr (SPARSE) {
+        if (warp == kProducerWarp) {
+            // bit i of qbits: query tile i's mask row has this key block set (and
+            // i is at or below the diagonal when causal); one ballot per 32 tiles
+            const uint8_t* m = p.blocks + bh * p.blocks_head_stride;
+            for (int w = 0; w * 32 < n_q; ++w) {
+                const int i = w * 32 + lane;
+                bool u = false;
+                if (i < n_q && (!CAUSAL || i >= kv_tile))
+                    u = m[static_cast<long long>(i) * p.n_kv + kv_tile] != 0;
+                const uint32_t bits = __ballot_sync(0xffffffffu, u);
+                if (lane == 0) sh.qbits[w] = bits;
+            }
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
     const Watchdog wd{p.err, &sh.abort_flag, p.wait_limit_ns};
     constexpr uint32_t FULL = 0xffffffffu;
+    if constexpr (SPARSE) {
+        int c = 0;
+        for (int w = 0; w * 32 < n_q; ++w) c += __popc(sh.qbits[w]);
+        n_steps = c;
+    }
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------- producer --
-        if (lane == 0) {
+        // a key tile that no query tile visits (block mask) loads nothing: its
+        // epilogue writes zero dK, dV over the K and V tiles
+        if (lane == 0 && (!SPARSE || n_steps > 0)) {
             mbar_arrive_expect_tx(bar_kv, 2 * L::kTile);
             for (int b = 0; b < L::kBoxes; ++b) {
                 tma_load_3d(sbase + L::kK + b * L::kBox, &tmK, bar_kv, b * 64, kv_start, bh);
                 tma_load_3d(sbase + L::kV + b * L::kBox, &tmV, bar_kv, b * 64, kv_start, bh);
             }
         }
+        int qsp = -1;  // block mask: the query tile of the last step
         for (int s = 0; s < n_steps; ++s) {
             const int st = s & 1;
             if (s >= 2 && !mbar_wait(bar_qe + 8 * st, ((s >> 1) - 1) & 1, wd, kSiteProd)) break;
-            const int q_start = (first + s) * kBQ;
+            int qtile = first + s;
+            if constexpr (SPARSE) {
+                qsp = next_set_bit(sh.qbits, nullptr, qsp + 1, n_q);
+                qtile = qsp;
+            }
+            const int q_start = qtile * kBQ;
             const int64_t row0 = static_cast<int64_t>(bh) * N;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -273,7 +311,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             const uint32_t do_lo0 = sw128_desc_lo(sbase + L::kStage0 + L::kTile, 16);
             const uint32_t do_mn0 = sw128_desc_lo(sbase + L::kStage0 + L::kTile, kLboMN);
             constexpr uint32_t kStageStep = L::kStageBytes >> 4;
-            bool ok = __all_sync(0xffffffffu, mbar_wait(bar_kv, 0, wd, kSiteMmaKV) &&
+            bool ok = (!SPARSE || n_steps > 0) &&
+                      __all_sync(0xffffffffu, mbar_wait(bar_kv, 0, wd, kSiteMmaKV) &&
                                                   mbar_wait(bar_qf, 0, wd, kSiteMmaQ));
             if (ok) {
                 tc_fence_after();
@@ -327,12 +366,18 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         // producer; waiting here keeps that wait off the softmax warps' path.
         if (lane == 0) {
             bool ok = true;
+            int qsp = -1;  // block mask: the query tile of the last step
             for (int s = 0; s < n_steps; ++s) {
                 const int st = s & 1;
+                int qtile = first + s;
+                if constexpr (SPARSE) {
+                    qsp = next_set_bit(sh.qbits, nullptr, qsp + 1, n_q);
+                    qtile = qsp;
+                }
                 if (ok) ok = mbar_wait(bar_sg, s & 1, wd, kSiteReduce);
                 if (ok) {
                     const uint32_t src = sbase + L::kStage0 + st * L::kStageBytes;
-                    const int q_start = (first + s) * kBQ;
+                    const int q_start = qtile * kBQ;
                     for (int b = 0; b < D / 32; ++b)
                         tma_reduce_add_3d(&tmdQacc, src + b * L::kBox, b * 32, q_start, bh);
                     bulk_commit();
@@ -359,9 +404,15 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         uint8_t* ds_row = smem + L::kDS + h * (128 * 128) + r * 128;
         constexpr int kDrainBoxes = D / 64;  // fp32 boxes of 32 columns per warpgroup
         bool ok = true;
+        int qsp = -1;  // block mask: the query tile of the last step
         for (int s = 0; s < n_steps; ++s) {
             const int st = s & 1;
-            const int q_start = (first + s) * kBQ;
+            int qtile = first + s;
+            if constexpr (SPARSE) {
+                qsp = next_set_bit(sh.qbits, nullptr, qsp + 1, n_q);
+                qtile = qsp;
+            }
+            const int q_start = qtile * kBQ;
             // P^T = exp2(c S^T - log2e LSE), bf16, over this warpgroup's S^T columns
             if (ok) ok = __all_sync(FULL, mbar_wait(bar_s, s & 1, wd, kSiteDsS) &&
                                               mbar_wait(bar_qf + 8 * st, (s >> 1) & 1, wd, kSiteDsQ));
@@ -486,8 +537,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int cc = 0; cc < D / 2; cc += 32) {
                     const int c0 = h * (D / 2) + cc;
                     uint32_t o[32];
-                    tmem_ld32(src + c0, o);
-                    tmem_ld_wait(o);
+                    if (!SPARSE || n_steps > 0) {
+                        tmem_ld32(src + c0, o);
+                        tmem_ld_wait(o);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = 0u;  // no query sees these keys
+                    }
                     const int box = c0 / 64;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -572,7 +628,7 @@ __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restric
     }
 }
 
-template <int D, bool CAUSAL, bool LOCAL = false>
+template <int D, bool CAUSAL, int MASK = kMaskNone>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     using L = BwdLayout<D>;
     const int64_t rows = static_cast<int64_t>(a.BH) * a.N;
@@ -599,7 +655,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
             !make_tile_map(&tdk, a.dK, BF, 2, D, a.N, a.BH, 64, kBK) ||
             !make_tile_map(&tdv, a.dV, BF, 2, D, a.N, a.BH, 64, kBK))
             return cudaErrorInvalidValue;
-        auto kern = fa_bwd_main_kernel<D, CAUSAL, LOCAL>;
+        auto kern = fa_bwd_main_kernel<D, CAUSAL, MASK>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
         if (e != cudaSuccess) return e;
         BwdParams p;
@@ -610,6 +666,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         p.scale_log2 = a.tau * kLog2e;
         p.tau = a.tau;
         p.window = (a.window > 0 && a.window < a.N) ? a.window : 0;
+        p.blocks = a.blocks;
+        p.blocks_head_stride = a.blocks_head_stride;
         p.err = a.err;
         p.wait_limit_ns = a.wait_limit_ns;
         dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(p.n_kv));
@@ -633,8 +691,16 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+    if (a.blocks) {
+        if (a.d == 64)
+            return a.causal ? launch_bwd_t<64, true, kMaskBlocks>(a, stream)
+                            : launch_bwd_t<64, false, kMaskBlocks>(a, stream);
+        return a.causal ? launch_bwd_t<128, true, kMaskBlocks>(a, stream)
+                        : launch_bwd_t<128, false, kMaskBlocks>(a, stream);
+    }
     if (a.causal && a.window > 0 && a.window < a.N)
-        return a.d == 64 ? launch_bwd_t<64, true, true>(a, stream) : launch_bwd_t<128, true, true>(a, stream);
+        return a.d == 64 ? launch_bwd_t<64, true, kMaskWindow>(a, stream)
+                         : launch_bwd_t<128, true, kMaskWindow>(a, stream);
     if (a.d == 64) return a.causal ? launch_bwd_t<64, true>(a, stream) : launch_bwd_t<64, false>(a, stream);
     return a.causal ? launch_bwd_t<128, true>(a, stream) : launch_bwd_t<128, false>(a, stream);
 }

@@ -43,6 +43,9 @@ constexpr int kMmaWarp = 9;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.44269504088896341f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
+// Which keys a query tile visits beyond causality.
+enum : int { kMaskNone = 0, kMaskWindow = 1, kMaskBlocks = 2 };
+constexpr int kMaskWords = kMaxMaskBlocks / 32;
 
 template <int D>
 struct FwdLayout {
@@ -68,6 +71,8 @@ struct FwdParams {
     unsigned int* err;
     unsigned long long wait_limit_ns;
     int window;  // causal sliding window in keys (0 = none)
+    const uint8_t* blocks;          // block mask [heads][n_kv][n_kv] (kMaskBlocks)
+    long long blocks_head_stride;   // bytes between heads' masks (0: one mask)
 };
 
 struct FwdShared {
@@ -79,6 +84,7 @@ struct FwdShared {
     uint64_t o_done[2];
     uint32_t tmem_base;
     int abort_flag;
+    uint32_t use[2][kMaskWords];  // kMaskBlocks: bit j of use[t] = tile t visits key block j
 };
 
 // Wait-site ids recorded in the error word.
@@ -117,13 +123,16 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
         mma_ts_warp<1>(tmem_o, tmem_p + k * 8, v_lo + ((k * 2048) >> 4), kDescHi, id);
 }
 
-// LOCAL: causal sliding window of p.window keys (only with CAUSAL).
-template <int D, bool CAUSAL, bool O32, bool LOCAL>
+// MASK: kMaskNone; kMaskWindow, a causal sliding window of p.window keys (only
+// with CAUSAL); kMaskBlocks, the block mask p.blocks (bf16 O only).
+template <int D, bool CAUSAL, bool O32, int MASK>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
               const FwdParams p) {
     using L = FwdLayout<D>;
+    constexpr bool LOCAL = MASK == kMaskWindow;
+    constexpr bool SPARSE = MASK == kMaskBlocks;
     extern __shared__ uint8_t smem_raw[];
     __shared__ FwdShared sh;
     const uint32_t raw = smem_addr(smem_raw);
@@ -147,10 +156,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int hi1 = q_start1 < N ? (CAUSAL ? min(n_kv, q_start1 / kBN + 1) : n_kv) : 0;
     const int lo0 = window > 0 ? max(0, q_start0 - window + 1) / kBN : 0;
     const int lo1 = window > 0 ? max(0, q_start1 - window + 1) / kBN : 0;
-    const int n_blk0 = hi0 - lo0;
-    const int n_blk1 = hi1 > 0 ? hi1 - lo1 : 0;
+    int n_blk0 = hi0 - lo0;
+    int n_blk1 = hi1 > 0 ? hi1 - lo1 : 0;
     const int jlo = lo0;
-    const int nb = max(hi0, hi1) - jlo;  // key blocks loaded
+    int nb = max(hi0, hi1) - jlo;  // key blocks loaded (with a block mask: counted below)
 
     const uint32_t bar_q = smem_addr(&sh.q_full);
     const uint32_t bar_kv_full = smem_addr(&sh.kv_full[0]);
@@ -183,23 +192,58 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tma_prefetch_map(&tmV);
         if (!O32) tma_prefetch_map(&tmO);
     }
+    if constexpr (SPARSE) {
+        if (warp == kProducerWarp) {
+            // bit j of use[t]: tile t's mask row has key block j set (and j is at or
+            // below the diagonal when causal); one ballot per 32 blocks
+            const uint8_t* m = p.blocks + bh * p.blocks_head_stride;
+            const int qb[2] = {q_start0 / kBN, q_start1 / kBN};
+            for (int w = 0; w * 32 < n_kv; ++w) {
+                const int j = w * 32 + lane;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    bool u = false;
+                    if ((t == 0 || q_start1 < N) && j < n_kv && (!CAUSAL || j <= qb[t]))
+                        u = m[static_cast<long long>(qb[t]) * n_kv + j] != 0;
+                    const uint32_t bits = __ballot_sync(0xffffffffu, u);
+                    if (lane == 0) sh.use[t][w] = bits;
+                }
+            }
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
     const Watchdog wd{p.err, &sh.abort_flag, p.wait_limit_ns};
+    if constexpr (SPARSE) {
+        int c0 = 0, c1 = 0, cu = 0;
+        for (int w = 0; w * 32 < n_kv; ++w) {
+            c0 += __popc(sh.use[0][w]);
+            c1 += __popc(sh.use[1][w]);
+            cu += __popc(sh.use[0][w] | sh.use[1][w]);
+        }
+        n_blk0 = c0;
+        n_blk1 = c1;
+        nb = cu;
+    }
 
     if (warp >= kProducerWarp) {
         if (warp == kProducerWarp) {
             // ------------------------------------------------------- producer --
-            if (lane == 0) {
-                uint32_t qbytes = L::kTileBytes * ((n_blk0 > 0) + (n_blk1 > 0));
+            // with a block mask, a tile that visits no key block loads no Q, and a
+            // pair that visits none loads nothing
+            if (lane == 0 && (!SPARSE || nb > 0)) {
+                const bool q0 = !SPARSE || n_blk0 > 0;
+                uint32_t qbytes = L::kTileBytes * (q0 + (n_blk1 > 0));
                 mbar_arrive_expect_tx(bar_q, qbytes);
                 for (int b = 0; b < L::kBoxes; ++b) {
-                    tma_load_3d(sbase + L::kQ0 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start0, bh);
+                    if (q0)
+                        tma_load_3d(sbase + L::kQ0 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start0, bh);
                     if (n_blk1 > 0)
                         tma_load_3d(sbase + L::kQ1 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start1, bh);
                 }
+                int jb = -1;  // block mask: the block being loaded
                 for (int ld = 0; ld < 2 * nb; ++ld) {
                     const int slot = ld % L::kStages;
                     if (ld >= L::kStages &&
@@ -207,10 +251,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         break;
                     const CUtensorMap* map = (ld & 1) ? &tmV : &tmK;
                     const uint32_t dst = sbase + L::kRing + slot * L::kTileBytes;
+                    int blk = jlo + (ld >> 1);
+                    if constexpr (SPARSE) {
+                        if ((ld & 1) == 0) jb = next_set_bit(sh.use[0], sh.use[1], jb + 1, n_kv);
+                        blk = jb;
+                    }
                     mbar_arrive_expect_tx(bar_kv_full + 8 * slot, L::kTileBytes);
                     for (int b = 0; b < L::kBoxes; ++b)
                         tma_load_3d(dst + b * L::kBoxBytes, map, bar_kv_full + 8 * slot, b * 64,
-                                    (jlo + (ld >> 1)) * kBN, bh);
+                                    blk * kBN, bh);
                 }
             }
         } else if (warp == kMmaWarp) {
@@ -224,103 +273,168 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const uint32_t klo0 = sw128_desc_lo(sbase + L::kRing, 16);          // K: K-major
                 const uint32_t vlo0 = sw128_desc_lo(sbase + L::kRing, 128 * 128);   // V: MN-major
                 constexpr uint32_t kSlot = L::kTileBytes >> 4;
-                const int lo[2] = {lo0, lo1};
-                const int hi[2] = {hi0, n_blk1 > 0 ? hi1 : 0};
-                bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteMmaQ) &&
-                                                      mbar_wait(bar_kv_full, 0, wd, kSiteMmaKV));
-                if (ok) {
-                    tc_fence_after();
-                    for (int t = 0; t < 2; ++t) {
-                        if (lo[t] == jlo && hi[t] > jlo) {
-                            issue_s<D>(tS[t], qlo[t], klo0);
-                            mma_commit_warp(bar_s + 8 * t);
+                if constexpr (SPARSE) {
+                    // walk the union of the two tiles' key blocks; tile t takes the
+                    // blocks whose bit is set in use[t]
+                    auto uses = [&](int t, int j) { return ((sh.use[t][j >> 5] >> (j & 31)) & 1u) != 0; };
+                    if (nb > 0) {
+                        bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteMmaQ) &&
+                                                              mbar_wait(bar_kv_full, 0, wd, kSiteMmaKV));
+                        int j = next_set_bit(sh.use[0], sh.use[1], 0, n_kv);
+                        if (ok) {
+                            tc_fence_after();
+#pragma unroll
+                            for (int t = 0; t < 2; ++t) {
+                                if (uses(t, j)) {
+                                    issue_s<D>(tS[t], qlo[t], klo0);
+                                    mma_commit_warp(bar_s + 8 * t);
+                                }
+                            }
+                            mma_commit_warp(bar_kv_empty);
                         }
-                    }
-                    mma_commit_warp(bar_kv_empty);
-                }
-                if constexpr (!LOCAL) {
-                    // every tile starts at key block 0: tile t takes blocks [0, hi[t])
-                    for (int j = 0; ok && j < nb; ++j) {
-                        const int lv = 2 * j + 1, lk = 2 * j + 2;
-                        const int sv = lv % L::kStages, sk = lk % L::kStages;
-                        if (!__all_sync(0xffffffffu,
-                                        mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1, wd, kSiteMmaKV))) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        bool k_ready = false;
-                        for (int t = 0; t < 2 && ok; ++t) {
-                            if (j >= hi[t]) continue;
-                            if (!__all_sync(0xffffffffu, mbar_wait(bar_p + 8 * t, j & 1, wd, kSiteMmaP))) {
+                        int cnt[2] = {0, 0};  // P.V products issued per tile
+                        for (int u = 0; ok && u < nb; ++u) {
+                            const int jn = next_set_bit(sh.use[0], sh.use[1], j + 1, n_kv);
+                            const int lv = 2 * u + 1, lk = 2 * u + 2;
+                            const int sv = lv % L::kStages, sk = lk % L::kStages;
+                            if (!__all_sync(0xffffffffu,
+                                            mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1, wd, kSiteMmaKV))) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
-                            issue_pv<D>(tO[t], tS[t], vlo0 + sv * kSlot, j > 0);
-                            mma_commit_warp(bar_o + 8 * t);
-                            if (j + 1 < hi[t]) {
-                                if (!k_ready) {
-                                    if (!__all_sync(0xffffffffu,
-                                                    mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1,
-                                                              wd, kSiteMmaKV))) {
-                                        ok = false;
-                                        break;
+                            bool k_ready = false;
+#pragma unroll
+                            for (int t = 0; t < 2; ++t) {
+                                if (ok && uses(t, j)) {
+                                    ok = __all_sync(0xffffffffu,
+                                                    mbar_wait(bar_p + 8 * t, cnt[t] & 1, wd, kSiteMmaP));
+                                    if (ok) {
+                                        tc_fence_after();
+                                        issue_pv<D>(tO[t], tS[t], vlo0 + sv * kSlot, cnt[t] > 0);
+                                        mma_commit_warp(bar_o + 8 * t);
                                     }
-                                    tc_fence_after();
-                                    k_ready = true;
+                                    ++cnt[t];
                                 }
-                                issue_s<D>(tS[t], qlo[t], klo0 + sk * kSlot);
+                                if (ok && jn < n_kv && uses(t, jn)) {
+                                    if (!k_ready) {
+                                        ok = __all_sync(0xffffffffu,
+                                                        mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1,
+                                                                  wd, kSiteMmaKV));
+                                        if (ok) tc_fence_after();
+                                        k_ready = true;
+                                    }
+                                    if (ok) {
+                                        issue_s<D>(tS[t], qlo[t], klo0 + sk * kSlot);
+                                        mma_commit_warp(bar_s + 8 * t);
+                                    }
+                                }
+                            }
+                            if (!ok) break;
+                            mma_commit_warp(bar_kv_empty + 8 * sv);
+                            if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
+                            j = jn;
+                        }
+                    }
+                } else {
+                    const int lo[2] = {lo0, lo1};
+                    const int hi[2] = {hi0, n_blk1 > 0 ? hi1 : 0};
+                    bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteMmaQ) &&
+                                                          mbar_wait(bar_kv_full, 0, wd, kSiteMmaKV));
+                    if (ok) {
+                        tc_fence_after();
+                        for (int t = 0; t < 2; ++t) {
+                            if (lo[t] == jlo && hi[t] > jlo) {
+                                issue_s<D>(tS[t], qlo[t], klo0);
                                 mma_commit_warp(bar_s + 8 * t);
                             }
                         }
-                        if (!ok) break;
-                        mma_commit_warp(bar_kv_empty + 8 * sv);
-                        if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
+                        mma_commit_warp(bar_kv_empty);
                     }
-                } else {
-                    // tile t takes blocks [lo[t], hi[t]); S of a tile's first block may
-                    // be issued while the other tile is still in its leading blocks
-                    for (int u = 0; ok && u < nb; ++u) {
-                        const int j = jlo + u;  // key block
-                        const int lv = 2 * u + 1, lk = 2 * u + 2;
-                        const int sv = lv % L::kStages, sk = lk % L::kStages;
-                        if (!__all_sync(0xffffffffu,
-                                        mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1, wd, kSiteMmaKV))) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        bool k_ready = false;
-                        // fully unrolled over the two tiles so the per-tile arrays stay in registers
-    #pragma unroll
-                        for (int t = 0; t < 2; ++t) {
-                            if (ok && j >= lo[t] && j < hi[t]) {
-                                ok = __all_sync(0xffffffffu,
-                                                mbar_wait(bar_p + 8 * t, (j - lo[t]) & 1, wd, kSiteMmaP));
-                                if (ok) {
-                                    tc_fence_after();
-                                    issue_pv<D>(tO[t], tS[t], vlo0 + sv * kSlot, j > lo[t]);
-                                    mma_commit_warp(bar_o + 8 * t);
-                                }
+                    if constexpr (!LOCAL) {
+                        // every tile starts at key block 0: tile t takes blocks [0, hi[t])
+                        for (int j = 0; ok && j < nb; ++j) {
+                            const int lv = 2 * j + 1, lk = 2 * j + 2;
+                            const int sv = lv % L::kStages, sk = lk % L::kStages;
+                            if (!__all_sync(0xffffffffu,
+                                            mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1, wd, kSiteMmaKV))) {
+                                ok = false;
+                                break;
                             }
-                            if (ok && j + 1 >= lo[t] && j + 1 < hi[t]) {
-                                if (!k_ready) {
-                                    ok = __all_sync(0xffffffffu,
-                                                    mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1,
-                                                              wd, kSiteMmaKV));
-                                    if (ok) tc_fence_after();
-                                    k_ready = true;
+                            tc_fence_after();
+                            bool k_ready = false;
+                            for (int t = 0; t < 2 && ok; ++t) {
+                                if (j >= hi[t]) continue;
+                                if (!__all_sync(0xffffffffu, mbar_wait(bar_p + 8 * t, j & 1, wd, kSiteMmaP))) {
+                                    ok = false;
+                                    break;
                                 }
-                                if (ok) {
+                                tc_fence_after();
+                                issue_pv<D>(tO[t], tS[t], vlo0 + sv * kSlot, j > 0);
+                                mma_commit_warp(bar_o + 8 * t);
+                                if (j + 1 < hi[t]) {
+                                    if (!k_ready) {
+                                        if (!__all_sync(0xffffffffu,
+                                                        mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1,
+                                                                  wd, kSiteMmaKV))) {
+                                            ok = false;
+                                            break;
+                                        }
+                                        tc_fence_after();
+                                        k_ready = true;
+                                    }
                                     issue_s<D>(tS[t], qlo[t], klo0 + sk * kSlot);
                                     mma_commit_warp(bar_s + 8 * t);
                                 }
                             }
+                            if (!ok) break;
+                            mma_commit_warp(bar_kv_empty + 8 * sv);
+                            if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
                         }
-                        if (!ok) break;
-                        mma_commit_warp(bar_kv_empty + 8 * sv);
-                        if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
+                    } else {
+                        // tile t takes blocks [lo[t], hi[t]); S of a tile's first block may
+                        // be issued while the other tile is still in its leading blocks
+                        for (int u = 0; ok && u < nb; ++u) {
+                            const int j = jlo + u;  // key block
+                            const int lv = 2 * u + 1, lk = 2 * u + 2;
+                            const int sv = lv % L::kStages, sk = lk % L::kStages;
+                            if (!__all_sync(0xffffffffu,
+                                            mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1, wd, kSiteMmaKV))) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            bool k_ready = false;
+                            // fully unrolled over the two tiles so the per-tile arrays stay in registers
+        #pragma unroll
+                            for (int t = 0; t < 2; ++t) {
+                                if (ok && j >= lo[t] && j < hi[t]) {
+                                    ok = __all_sync(0xffffffffu,
+                                                    mbar_wait(bar_p + 8 * t, (j - lo[t]) & 1, wd, kSiteMmaP));
+                                    if (ok) {
+                                        tc_fence_after();
+                                        issue_pv<D>(tO[t], tS[t], vlo0 + sv * kSlot, j > lo[t]);
+                                        mma_commit_warp(bar_o + 8 * t);
+                                    }
+                                }
+                                if (ok && j + 1 >= lo[t] && j + 1 < hi[t]) {
+                                    if (!k_ready) {
+                                        ok = __all_sync(0xffffffffu,
+                                                        mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1,
+                                                                  wd, kSiteMmaKV));
+                                        if (ok) tc_fence_after();
+                                        k_ready = true;
+                                    }
+                                    if (ok) {
+                                        issue_s<D>(tS[t], qlo[t], klo0 + sk * kSlot);
+                                        mma_commit_warp(bar_s + 8 * t);
+                                    }
+                                }
+                            }
+                            if (!ok) break;
+                            mma_commit_warp(bar_kv_empty + 8 * sv);
+                            if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
+                        }
                     }
                 }
             }
@@ -342,8 +456,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         float m_used = -INFINITY;
         float l = 0.f, l_mma = 0.f;
         bool ok = true;
+        int jsp = -1;  // block mask: the last key block visited
         for (int jj = 0; jj < nbt; ++jj) {
-            const int j = lot + jj;  // key block
+            int j = lot + jj;  // key block
+            if constexpr (SPARSE) {
+                jsp = next_set_bit(sh.use[t], nullptr, jsp + 1, n_kv);
+                j = jsp;
+            }
             // wait results are made warp-uniform: tcgen05.ld/st are warp-collective
             if (!__all_sync(0xffffffffu, mbar_wait(my_s, jj & 1, wd, kSiteSoftS))) {
                 ok = false;
@@ -488,7 +607,25 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             }
             if (row < N) p.LSE[bh_row] = (m_used + __log2f(l)) * kLn2;
         }
-        if (!O32 && nbt > 0) {
+        bool empty_tile = false;
+        if constexpr (SPARSE) {
+            // a tile whose mask row visits no key block: every row is the empty
+            // sum, O = 0 and LSE = -inf (its Q smem was never loaded: stage zeros there)
+            empty_tile = nbt == 0 && q_start < N;
+            if (empty_tile) {
+                uint8_t* stage = smem + (t ? L::kQ1 : L::kQ0);
+#pragma unroll
+                for (int b = 0; b < L::kBoxes; ++b)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(stage + b * L::kBoxBytes + r * 128 + c * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                fence_async_shared();
+                if (row < N) p.LSE[static_cast<int64_t>(bh) * N + row] = -INFINITY;
+                epi = true;
+            }
+        }
+        if (!O32 && (nbt > 0 || empty_tile)) {
             // every thread of the warpgroup reaches this barrier, even after an abort
             named_bar_sync(1 + t, 128);
             if (r == 0 && epi) {
@@ -511,7 +648,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
 }
 
-template <int D, bool CAUSAL, bool O32, bool LOCAL = false>
+template <int D, bool CAUSAL, bool O32, int MASK = kMaskNone>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     using L = FwdLayout<D>;
     CUtensorMap tq, tk, tv, to;
@@ -524,7 +661,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     } else if (!make_tile_map(&to, a.O, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.BH, 64, kBM)) {
         return cudaErrorInvalidValue;
     }
-    auto kern = fa_fwd_kernel<D, CAUSAL, O32, LOCAL>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, O32, MASK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
     if (e != cudaSuccess) return e;
     FwdParams p;
@@ -532,6 +669,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     p.O32 = O32 ? static_cast<float*>(a.O) : nullptr;
     p.N = a.N;
     p.window = (a.window > 0 && a.window < a.N) ? a.window : 0;
+    p.blocks = a.blocks;
+    p.blocks_head_stride = a.blocks_head_stride;
     p.n_pairs = (a.N + 2 * kBM - 1) / (2 * kBM);
     p.scale_log2 = a.tau * kLog2e;
     p.err = a.err;
@@ -547,9 +686,17 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+    if (a.blocks) {
+        if (a.o32) return cudaErrorInvalidValue;
+        if (a.d == 64)
+            return a.causal ? launch_fwd_t<64, true, false, kMaskBlocks>(a, stream)
+                            : launch_fwd_t<64, false, false, kMaskBlocks>(a, stream);
+        return a.causal ? launch_fwd_t<128, true, false, kMaskBlocks>(a, stream)
+                        : launch_fwd_t<128, false, false, kMaskBlocks>(a, stream);
+    }
     if (a.causal && !a.o32 && a.window > 0 && a.window < a.N)
-        return a.d == 64 ? launch_fwd_t<64, true, false, true>(a, stream)
-                         : launch_fwd_t<128, true, false, true>(a, stream);
+        return a.d == 64 ? launch_fwd_t<64, true, false, kMaskWindow>(a, stream)
+                         : launch_fwd_t<128, true, false, kMaskWindow>(a, stream);
     if (a.d == 64) {
         if (a.causal) return a.o32 ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, true, false>(a, stream);
         return a.o32 ? launch_fwd_t<64, false, true>(a, stream) : launch_fwd_t<64, false, false>(a, stream);

@@ -8,6 +8,11 @@
 
 namespace fa {
 
+// Block masks (block-sparse attention): one byte per [128 query x 128 key] block,
+// at most kMaxMaskBlocks blocks per row (so N <= 131072).
+constexpr int kMaskBlockEdge = 128;
+constexpr int kMaxMaskBlocks = 1024;
+
 // Arguments of one forward launch (device pointers, validated by the caller).
 struct FwdArgs {
     const void* Q;
@@ -19,6 +24,8 @@ struct FwdArgs {
     float tau;
     bool causal;
     int window;       // causal sliding window in keys (0 = none)
+    const uint8_t* blocks = nullptr;  // block mask [heads][nb][nb] (device) or null
+    long long blocks_head_stride = 0;  // bytes between heads' masks (0: one mask)
     bool o32;
     unsigned int* err;
     unsigned long long wait_limit_ns;
@@ -43,6 +50,8 @@ struct BwdArgs {
     float tau;
     bool causal;
     int window;     // causal sliding window in keys (0 = none)
+    const uint8_t* blocks = nullptr;  // block mask [heads][nb][nb] (device) or null
+    long long blocks_head_stride = 0;  // bytes between heads' masks (0: one mask)
     unsigned int* err;
     unsigned long long wait_limit_ns;
     cudaEvent_t ev_start;  // optional: recorded around the main kernel

@@ -485,4 +485,15 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return d;
 }
 
+// Smallest index j in [from, n) whose bit is set in a | b (b may be null), or n.
+// Bits at or past n must be clear.
+__device__ __forceinline__ int next_set_bit(const uint32_t* a, const uint32_t* b, int from, int n) {
+    for (int w = from >> 5; w * 32 < n; ++w) {
+        uint32_t m = a[w] | (b ? b[w] : 0u);
+        if (w == (from >> 5)) m &= 0xffffffffu << (from & 31);
+        if (m) return w * 32 + __ffs(m) - 1;
+    }
+    return n;
+}
+
 }  // namespace fa

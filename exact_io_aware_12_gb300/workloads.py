@@ -118,3 +118,34 @@ def sample_rows(w: Workload, per_head: Optional[int] = None) -> np.ndarray:
         head = np.union1d(fixed_arr, extra)
         rows.append(bh * N + head)
     return np.concatenate(rows).astype(np.int64)
+
+
+def local_global_block_mask(n_blocks: int, local: int, anchors: int, heads: int = 1,
+                            extra: float = 0.0, seed: int = 0) -> np.ndarray:
+    """Seeded block mask, uint8 [heads, n_blocks, n_blocks], of the sparse
+    pattern sketched in "Atencao eficiente - FlashAttention, sparse e hibrida",
+    section "Sparse e hibrida" (a local window plus global anchor tokens): row
+    block i sees key blocks [i - local + 1, i] and the first ``anchors`` key
+    blocks; ``extra`` sets that fraction of the remaining blocks at random,
+    drawn per head from ``numpy.random.default_rng(seed)``."""
+    m = np.zeros((heads, n_blocks, n_blocks), dtype=np.uint8)
+    i = np.arange(n_blocks)[:, None]
+    j = np.arange(n_blocks)[None, :]
+    m[:] = ((j <= i) & (j > i - local)) | (j < anchors)
+    if extra > 0:
+        g = np.random.default_rng(seed)
+        m |= (g.random(m.shape) < extra).astype(np.uint8)
+    return m
+
+
+def random_block_mask(n_blocks: int, heads: int, density: float, seed: int,
+                      empty_rows: int = 0) -> np.ndarray:
+    """Seeded random block mask, uint8 [heads, n_blocks, n_blocks]: each entry
+    set with probability ``density``; then ``empty_rows`` row blocks per head
+    (chosen from the same generator) are cleared entirely."""
+    g = np.random.default_rng(seed)
+    m = (g.random((heads, n_blocks, n_blocks)) < density).astype(np.uint8)
+    for h in range(heads):
+        for r in g.choice(n_blocks, size=min(empty_rows, n_blocks), replace=False):
+            m[h, r] = 0
+    return m

@@ -147,8 +147,44 @@ FA_API fa_status fa_bwd_window(const void* Q, const void* K, const void* V, cons
                                float tau, int window, void* stream);
 
 /*
+ * Block-sparse attention, forward ("FlashAttention e o gargalo real de
+ * inferencia", section "o que isso custou": the block-sparse variant skips
+ * blocks, an approximation by design; "Atencao eficiente - FlashAttention,
+ * sparse e hibrida", section "Sparse e hibrida": each token attends to a
+ * subset, e.g. a local window plus global anchor tokens).
+ *
+ * block_mask: DEVICE pointer to bytes [mask_heads][nb][nb], nb = ceil(N / 128)
+ * (FA_BLOCK_MASK_EDGE), row-major: entry [h][i][j] nonzero means the queries
+ * of 128-row block i of head h see the keys of 128-key block j.  mask_heads
+ * is 1 (one mask for every batch and head) or B*H (head bh = b*H + h uses
+ * mask bh); anything else is FA_ERR_INVALID_ARG.  With causal = 1 a key is
+ * visible only if it is also at or before the query.  Blocks that are not set
+ * are never loaded.  A row that sees no key is the empty sum: O = 0 and
+ * LSE = -inf.  The mask is read on the stream; it must stay valid until the
+ * call's work is done and must not overlap O or LSE.  N <= FA_BLOCK_MASK_MAX_N
+ * (else FA_ERR_UNSUPPORTED).  Other buffers and conventions as fa_fwd.
+ */
+#define FA_BLOCK_MASK_EDGE 128
+#define FA_BLOCK_MASK_MAX_N 131072
+FA_API fa_status fa_fwd_blocks(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                               int B, int H, int N, int d, float tau, int causal,
+                               const unsigned char* block_mask, int mask_heads, void* stream);
+
+/*
+ * Block-sparse backward: fa_bwd for the mask of fa_fwd_blocks (LSE must come
+ * from fa_fwd_blocks with the same mask).  Rows that see no key get dQ = 0;
+ * keys that no query sees get dK = dV = 0.  Same workspace rules as fa_bwd;
+ * the mask must not overlap dQ, dK, dV or the workspace.
+ */
+FA_API fa_status fa_bwd_blocks(const void* Q, const void* K, const void* V, const void* O,
+                               const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                               void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                               float tau, int causal, const unsigned char* block_mask,
+                               int mask_heads, void* stream);
+
+/*
  * Kernel timing hook.  With both events non-NULL (cudaEvent_t created by the
- * caller), every later fa_fwd / fa_fwd_o32 / fa_bwd call made from the
+ * caller), every later forward or backward call made from the
  * calling host thread records `start` on its stream right before the
  * attention kernel proper (the forward kernel; the backward's main kernel,
  * after its D/zeroing pre-kernel) and `stop` right after it, so the caller
