@@ -13,7 +13,8 @@ Every function takes arrays shaped ``[BH, N, d]`` (or ``[B, H, N, d]``; only
 the trailing two axes matter) in float64, C-contiguous.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``,
-``tests/test_oracle_window_pins.py`` and ``tests/test_oracle_blocks_pins.py``
+``tests/test_oracle_window_pins.py``, ``tests/test_oracle_blocks_pins.py`` and
+``tests/test_oracle_decode_pins.py``
 (closed forms, hand-worked golden values, finite differences, invariants,
 brute force on tiny inputs and an independent transcription of the pages'
 blocked loop).
@@ -100,6 +101,9 @@ def _load():
         lib.ora_attn_bwd_blocks.restype = None
         lib.ora_attn_bwd_blocks.argtypes = [dp, dp, dp, dp, i64, i64, i64, ctypes.c_double, ci,
                                             u8, i64, i64, dp, dp, dp, dp, dp, dp]
+        lib.ora_attn_fwd_decode.restype = None
+        lib.ora_attn_fwd_decode.argtypes = [dp, dp, dp, i64, i64, i64, i64, ctypes.c_double,
+                                            ctypes.c_int, dp, dp]
         _lib = lib
         return lib
 
@@ -228,6 +232,24 @@ def fwd_rows(q, k, v, tau: float, causal: bool, rows, window=None, blocks=None, 
     else:
         _load().ora_attn_fwd_rows_window(_ptr(q), _ptr(k), _ptr(v), BH, N, d, float(tau), w,
                                          rp, r.size, _ptr(O), _ptr(L))
+    return O, L
+
+
+def fwd_decode(q, k, v, tau: float, causal: bool):
+    """Decode forward: q [..., Nq, d] against k, v [..., Nk, d] (same leading
+    axes).  With causal, query i is position Nk - Nq + i and sees keys
+    j <= i + Nk - Nq.  Returns (O [..., Nq, d], LSE [..., Nq])."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    BH, Nq, d = _dims(q)
+    BHk, Nk, dk = _dims(k)
+    if BHk != BH or dk != d or v.shape != k.shape:
+        raise ValueError("q, k, v must share leading axes and d; k and v the same shape")
+    if causal and Nq > Nk:
+        raise ValueError("causal decode needs Nq <= Nk")
+    O = np.empty_like(q)
+    L = np.empty(q.shape[:-1], dtype=np.float64)
+    _load().ora_attn_fwd_decode(_ptr(q), _ptr(k), _ptr(v), BH, Nq, Nk, d, float(tau), int(causal),
+                                _ptr(O), _ptr(L))
     return O, L
 
 

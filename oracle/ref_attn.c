@@ -42,6 +42,11 @@
  *     blocks; key j is visible from query i only if mask[i / blk][j / blk] is
  *     nonzero (and j <= i when causal).  A row that sees no key is an empty
  *     sum: O_i = 0, LSE_i = -inf, and it contributes nothing to any gradient;
+ *   - decode ("Atencao eficiente - FlashAttention, sparse e hibrida", box
+ *     "FlashAttention nao acelera o decode token a token": each decode step
+ *     brings one new query row that reads the whole KV cache): Nq query rows
+ *     against Nk >= Nq cached keys, the queries being the last Nq positions of
+ *     the sequence, so with causal query i sees keys j <= i + (Nk - Nq);
  *   - LSE is in natural-log units of the tau-scaled scores;
  *   - the backward is the analytic gradient of O with respect to Q, K, V for
  *     an upstream gradient dO, with the softmax Jacobian written out as
@@ -64,7 +69,8 @@
 
 /* Which keys each query sees. */
 typedef struct {
-    int causal;            /* only keys j <= i */
+    int causal;            /* only keys j <= i + offset */
+    int64_t offset;        /* causal offset: Nk - Nq for decode, 0 when square */
     int64_t window;        /* > 0: only the `window` most recent keys, i - window < j */
     const uint8_t* blocks; /* NULL, or block masks [heads][nqb][nkb] (nonzero = visible) */
     int64_t blk;           /* edge of a mask block, in rows and in keys */
@@ -75,7 +81,7 @@ typedef struct {
 /* Key j is visible from query i of head bh. */
 static int visible(const Visibility* vs, int64_t bh, int64_t i, int64_t j)
 {
-    if (vs->causal && j > i) return 0;
+    if (vs->causal && j > i + vs->offset) return 0;
     if (vs->window > 0 && j <= i - vs->window) return 0;
     if (vs->blocks && !vs->blocks[bh * vs->head_stride + (i / vs->blk) * vs->nkb + j / vs->blk])
         return 0;
@@ -316,7 +322,7 @@ static void attn_bwd(const double* Q, const double* K, const double* V,
  * ceil(N / blk), mask_heads 1 = one mask for every head, else BH). */
 static Visibility plain_vis(int causal, int64_t window)
 {
-    Visibility vs = {causal, window, NULL, 1, 0, 0};
+    Visibility vs = {causal, 0, window, NULL, 1, 0, 0};
     return vs;
 }
 
@@ -324,7 +330,7 @@ static Visibility block_vis(int causal, const uint8_t* blocks, int64_t blk, int6
                             int64_t N)
 {
     int64_t nb = (N + blk - 1) / blk;
-    Visibility vs = {causal, 0, blocks, blk, nb, mask_heads == 1 ? 0 : nb * nb};
+    Visibility vs = {causal, 0, 0, blocks, blk, nb, mask_heads == 1 ? 0 : nb * nb};
     return vs;
 }
 
@@ -422,4 +428,28 @@ void ora_attn_bwd_blocks(const double* Q, const double* K, const double* V, cons
 {
     Visibility vs = block_vis(causal, blocks, blk, mask_heads, N);
     attn_bwd(Q, K, V, dO, BH, N, d, tau, &vs, dQ, dK, dV, O_out, LSE_out, D_out);
+}
+
+/*
+ * Decode forward: Nq query rows per head ([BH][Nq][d]) against Nk cached keys
+ * and values ([BH][Nk][d]); with causal, query i is at position Nk - Nq + i
+ * and sees keys j <= i + (Nk - Nq).  Outputs O [BH][Nq][d], LSE [BH][Nq].
+ */
+void ora_attn_fwd_decode(const double* Q, const double* K, const double* V, int64_t BH,
+                         int64_t Nq, int64_t Nk, int64_t d, double tau, int causal,
+                         double* O, double* LSE)
+{
+    Visibility vs = {causal, Nk - Nq, 0, NULL, 1, 0, 0};
+    int64_t rows = BH * Nq;
+#pragma omp parallel
+    {
+        double* p = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < rows; ++r) {
+            int64_t bh = r / Nq, i = r % Nq;
+            row_forward(Q + r * d, K + bh * Nk * d, V + bh * Nk * d, &vs, bh, i, Nk, d, tau,
+                        p, O + r * d, LSE + r);
+        }
+        free(p);
+    }
 }

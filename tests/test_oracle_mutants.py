@@ -14,12 +14,19 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "ref_attn.c")
 PIN_FILES = [os.path.join(ROOT, "tests", f)
-             for f in ("test_oracle_pins.py", "test_oracle_window_pins.py", "test_oracle_blocks_pins.py")]
+             for f in ("test_oracle_pins.py", "test_oracle_window_pins.py", "test_oracle_blocks_pins.py",
+                       "test_oracle_decode_pins.py")]
 
 MUTANTS = {
     "scores_without_tau": ("p[j] = tau * dot(q, K + j * d, d);", "p[j] = dot(q, K + j * d, d);"),
-    "causal_mask_reversed": ("if (vs->causal && j > i) return 0;", "if (vs->causal && j < i) return 0;"),
-    "causal_mask_strict": ("if (vs->causal && j > i) return 0;", "if (vs->causal && j >= i && i > 0) return 0;"),
+    "causal_mask_reversed": ("if (vs->causal && j > i + vs->offset) return 0;",
+                             "if (vs->causal && j < i + vs->offset) return 0;"),
+    "causal_mask_strict": ("if (vs->causal && j > i + vs->offset) return 0;",
+                           "if (vs->causal && j >= i + vs->offset && i > 0) return 0;"),
+    "decode_offset_sign": ("if (vs->causal && j > i + vs->offset) return 0;",
+                           "if (vs->causal && j > i - vs->offset) return 0;"),
+    "decode_offset_ignored": ("if (vs->causal && j > i + vs->offset) return 0;",
+                              "if (vs->causal && j > i) return 0;"),
     "window_off_by_one": ("if (vs->window > 0 && j <= i - vs->window) return 0;",
                           "if (vs->window > 0 && j < i - vs->window) return 0;"),
     "window_ignored": ("if (vs->window > 0 && j <= i - vs->window) return 0;",
