@@ -303,6 +303,7 @@ def run_ours(args):
                   if args.window > 0 and w.causal else None)
     blocks_leg = (measure_blocks(w, q, k, v, do, dev, min(args.steps, 20), peak)
                   if args.blocks and w.causal else None)
+    decode_leg = measure_decode(dev, min(args.steps, 20), peaks) if args.decode else None
     e2e = run_e2e(args, w, x, dev, f_step) if not args.no_e2e else None
     cpu = run_cpu_baseline(w, budget_s=args.cpu_seconds) if (rank == 0 and not args.no_cpu) else None
 
@@ -330,6 +331,7 @@ def run_ours(args):
         "roofline": roofline,
         "sliding_window": window_leg,
         "block_sparse": blocks_leg,
+        "decode": decode_leg,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 4 * args.steps,
@@ -430,6 +432,48 @@ def measure_blocks(w, q, k, v, do, dev, steps, peak):
     return {"mask": "per head: 4 local + 2 anchor blocks of 128, 2% random extra (seed 3)",
             "causal_work_fraction": round(ff / dense, 4),
             **measure_variant(w, q, k, v, do, dev, steps, peak, ff, blocks=mt)}
+
+
+def measure_decode(dev, steps, peaks):
+    """Decode step (fa_fwd_decode: split kernel + combine kernel) on the decode
+    workload: CUDA-event time around both kernels, and GB/s of the algorithmic
+    bytes (Q, K, V read once; O and LSE written once) against the measured HBM
+    copy bandwidth.  K and V (2.1 GB) exceed L2; L2 is flushed anyway."""
+    import torch
+    from exact_io_aware_12_gb300 import api, _lib
+    from exact_io_aware_12_gb300.workloads import DECODE_BY_NAME, draw_decode
+
+    w = DECODE_BY_NAME["decode_b8h16_nq1_nk32768_d128"]
+    x = draw_decode(w.B, w.H, w.Nq, w.Nk, w.d, w.seed)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    need = api.decode_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        api.fwd_decode(q, k, v, w.causal, w.tau, out=o, lse=lse, workspace=ws)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for e in sum(ev, []):
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        flush.fill_(float(i))
+        _lib.check(_lib.fa_set_timing_events(ev[i][0].cuda_event, ev[i][1].cuda_event), "timing")
+        api.fwd_decode(q, k, v, w.causal, w.tau, out=o, lse=lse, workspace=ws)
+        _lib.check(_lib.fa_set_timing_events(None, None), "timing")
+    torch.cuda.synchronize(dev)
+    if api.last_device_error(dev) != _lib.FA_OK:
+        raise RuntimeError("kernel watchdog fired in the decode leg")
+    ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    nbytes = 2 * (q.numel() + k.numel() + v.numel() + o.numel()) + 4 * lse.numel()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    return {"workload": w.name, "steps": steps, "ms": round(ms, 4),
+            "bytes": nbytes, "gbs": round(gbs, 1), "peak_gbs": peak,
+            "frac": round(gbs / peak, 4), "bound": "hbm",
+            "kernels": "fa_decode_split_kernel" + (" + fa_decode_combine_kernel" if need else "")}
 
 
 def run_e2e(args, w, x, dev, f_step):
@@ -569,6 +613,8 @@ def main(argv=None):
                     help="also time the causal sliding-window kernels with this window (0: skip)")
     ap.add_argument("--no-blocks", dest="blocks", action="store_false",
                     help="skip the block-sparse leg")
+    ap.add_argument("--no-decode", dest="decode", action="store_false",
+                    help="skip the decode leg")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

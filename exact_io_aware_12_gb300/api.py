@@ -139,6 +139,43 @@ def bwd(q, k, v, o, do, lse, causal: bool, tau: Optional[float] = None,
     return dq, dk, dv
 
 
+def decode_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    return _lib.fa_decode_workspace_size(B, H, Nq, Nk, d)
+
+
+def fwd_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool,
+               tau: Optional[float] = None, out: Optional[torch.Tensor] = None,
+               lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None):
+    """Decode forward (fa_fwd_decode): q [B, H, Nq, d] (1 <= Nq <= 8) against
+    the KV cache k, v [B, H, Nk, d]; with ``causal`` the queries are the last Nq
+    positions.  Returns (O bf16 [B, H, Nq, d], LSE fp32 [B, H, Nq]).  The
+    split workspace is allocated with torch when not given."""
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, Nq, d] queries")
+    B, H, Nq, d = q.shape
+    _check_inputs(k, v)
+    for t in (q, k, v):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("inputs must be contiguous CUDA bf16 tensors")
+    if k.shape[:2] != (B, H) or k.shape[3] != d or k.device != q.device:
+        raise ValueError("k, v must be [B, H, Nk, d] on q's device")
+    Nk = k.shape[2]
+    tau = 1.0 / math.sqrt(d) if tau is None else float(tau)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    need = decode_workspace_bytes(B, H, Nq, Nk, d)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wp, wn = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
+    code = _lib.fa_fwd_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr(), B, H, Nq, Nk, d, tau, int(bool(causal)), wp, wn,
+                              _stream_handle(q.device))
+    _lib.check(code, "fa_fwd_decode")
+    return out, lse
+
+
 def last_device_error(device: Optional[torch.device] = None) -> int:
     device = device or torch.device("cuda", torch.cuda.current_device())
     return _lib.fa_last_device_error(_stream_handle(device))

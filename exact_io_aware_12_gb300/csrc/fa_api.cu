@@ -350,6 +350,85 @@ fa_status fa_bwd_blocks(const void* Q, const void* K, const void* V, const void*
                       causal, 0, stream, block_mask, mask_heads);
 }
 
+size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d) {
+    if (B <= 0 || H <= 0 || Nq <= 0 || Nq > 8 || Nk <= 0 || (d != 64 && d != 128)) return 0;
+    const long long bh = static_cast<long long>(B) * H;
+    if (bh > INT_MAX) return 0;
+    int splits = 1, chunk = 0;
+    decode_plan(static_cast<int>(bh), Nk, &splits, &chunk);
+    if (splits <= 1) return 0;
+    const size_t rows = static_cast<size_t>(bh) * Nq;
+    return round256(static_cast<size_t>(splits) * rows * (d + 2) * sizeof(float));
+}
+
+fa_status fa_fwd_decode(const void* Q, const void* K, const void* V, void* O, float* LSE, int B,
+                        int H, int Nq, int Nk, int d, float tau, int causal, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d < 0) return FA_ERR_INVALID_ARG;
+    if (!(std::isfinite(tau) && tau > 0.f)) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (B == 0 || H == 0 || Nq == 0) return FA_OK;
+    if (Nk == 0 || (causal && Nq > Nk)) return FA_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || Nq > 8) return FA_ERR_UNSUPPORTED;
+    const long long bh = static_cast<long long>(B) * H;
+    if (bh > INT_MAX) return FA_ERR_UNSUPPORTED;
+    int splits = 1, chunk = 0;
+    decode_plan(static_cast<int>(bh), Nk, &splits, &chunk);
+    if (splits > 65535) return FA_ERR_UNSUPPORTED;
+    const void* ptrs[] = {Q, K, V, O, LSE};
+    for (const void* p : ptrs)
+        if (p == nullptr || !aligned16(p)) return FA_ERR_INVALID_ARG;
+    if (workspace != nullptr && !aligned16(workspace)) return FA_ERR_INVALID_ARG;
+    const size_t qb = static_cast<size_t>(bh) * Nq * d * 2, kb = static_cast<size_t>(bh) * Nk * d * 2;
+    const size_t lb = static_cast<size_t>(bh) * Nq * 4;
+    const void* ins[] = {Q, K, V};
+    const size_t in_bytes[] = {qb, kb, kb};
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(O, qb, ins[i], in_bytes[i]) || overlaps(LSE, lb, ins[i], in_bytes[i]))
+            return FA_ERR_INVALID_ARG;
+    if (overlaps(O, qb, LSE, lb)) return FA_ERR_INVALID_ARG;
+    const size_t need = fa_decode_workspace_size(B, H, Nq, Nk, d);
+    if (workspace != nullptr && need > 0) {
+        if (workspace_bytes < need) return FA_ERR_WORKSPACE;
+        const void* all[] = {Q, K, V, O, LSE};
+        const size_t all_bytes[] = {qb, kb, kb, qb, lb};
+        for (int i = 0; i < 5; ++i)
+            if (overlaps(workspace, need, all[i], all_bytes[i])) return FA_ERR_INVALID_ARG;
+    }
+    fa_status s = FA_OK;
+    DeviceInfo* di = current_device(&s);
+    if (!di) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void* ws = need > 0 ? workspace : nullptr;
+    const bool own = need > 0 && workspace == nullptr;
+    if (own && cudaMallocAsync(&ws, need, st) != cudaSuccess) {
+        cudaGetLastError();
+        return FA_ERR_CUDA;
+    }
+    DecArgs a;
+    a.Q = Q;
+    a.K = K;
+    a.V = V;
+    a.O = O;
+    a.LSE = LSE;
+    a.workspace = static_cast<float*>(ws);
+    a.BH = static_cast<int>(bh);
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.d = d;
+    a.tau = tau;
+    a.causal = causal != 0;
+    a.splits = splits;
+    a.chunk = chunk;
+    a.err = di->err_word;
+    a.wait_limit_ns = g_wait_limit_ns.load();
+    a.ev_start = t_ev_start;
+    a.ev_stop = t_ev_stop;
+    const cudaError_t e = launch_decode(a, st);
+    if (own) cudaFreeAsync(ws, st);
+    return map_cuda(e);
+}
+
 const char* fa_status_string(fa_status s) {
     switch (s) {
         case FA_OK: return "FA_OK";

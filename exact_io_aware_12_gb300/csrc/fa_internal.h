@@ -58,6 +58,28 @@ struct BwdArgs {
     cudaEvent_t ev_stop;
 };
 
+// Arguments of one decode forward (split kernel + combine kernel).
+struct DecArgs {
+    const void* Q;    // bf16 [BH][Nq][d]
+    const void* K;    // bf16 [BH][Nk][d]
+    const void* V;
+    void* O;          // bf16 [BH][Nq][d]
+    float* LSE;       // fp32 [BH][Nq]
+    float* workspace; // splits > 1: partials (decode_workspace_bytes)
+    int BH, Nq, Nk, d;
+    float tau;
+    bool causal;
+    int splits, chunk;  // from decode_plan
+    unsigned int* err;
+    unsigned long long wait_limit_ns;
+    cudaEvent_t ev_start;  // optional: recorded around the two kernels
+    cudaEvent_t ev_stop;
+};
+
+// How the decode forward cuts the KV cache: `splits` chunks of `chunk` keys
+// (a multiple of 64).  Depends only on its arguments.
+void decode_plan(int BH, int Nk, int* splits, int* chunk);
+
 // Encodes a 3-D tiled tensor map over a contiguous [BH][N][cols] tensor with
 // a {box_cols, box_rows, 1} box and the 128-byte swizzle (box_cols * esize
 // must be 128).  Returns false if the driver rejects it.
@@ -66,6 +88,7 @@ bool make_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const DecArgs& a, cudaStream_t stream);
 cudaError_t launch_watchdog_selftest(unsigned int* err, unsigned long long limit_ns,
                                      cudaStream_t stream);
 

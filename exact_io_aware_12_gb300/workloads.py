@@ -149,3 +149,40 @@ def random_block_mask(n_blocks: int, heads: int, density: float, seed: int,
         for r in g.choice(n_blocks, size=min(empty_rows, n_blocks), replace=False):
             m[h, r] = 0
     return m
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """A decode step: Nq new query rows per (batch, head) against an Nk-key KV
+    cache.  Inputs: one CPU generator seeded with ``seed``, Q then K then V as
+    float32 N(0, 1), rounded to bf16."""
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    causal: bool
+    seed: int
+
+    @property
+    def tau(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+
+DECODE_WORKLOADS: List[DecodeWorkload] = [
+    # one new token per sequence, 8 sequences x 16 heads reading a 32k-token cache (2.1 GB of K, V)
+    DecodeWorkload("decode_b8h16_nq1_nk32768_d128", 8, 16, 1, 32768, 128, True, 10),
+    # 4 tokens per step (draft tokens checked together) against a 128k-token cache
+    DecodeWorkload("decode_b1h8_nq4_nk131072_d128_causal", 1, 8, 4, 131072, 128, True, 11),
+]
+DECODE_BY_NAME: Dict[str, DecodeWorkload] = {w.name: w for w in DECODE_WORKLOADS}
+
+
+def draw_decode(B: int, H: int, Nq: int, Nk: int, d: int, seed: int) -> Dict[str, torch.Tensor]:
+    """Seeded bf16 CPU tensors q [B, H, Nq, d], k and v [B, H, Nk, d]."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    q = torch.randn((B, H, Nq, d), generator=g, dtype=torch.float32)
+    k = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32)
+    return {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16)}

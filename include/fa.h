@@ -183,6 +183,30 @@ FA_API fa_status fa_bwd_blocks(const void* Q, const void* K, const void* V, cons
                                int mask_heads, void* stream);
 
 /*
+ * Decode forward: Nq new query rows per (batch, head) against a KV cache of Nk
+ * keys ("Atencao eficiente - FlashAttention, sparse e hibrida", box
+ * "FlashAttention nao acelera o decode token a token": each decode step brings
+ * one new query row that reads the whole KV cache, so the step is bound by
+ * memory bandwidth).  Same result as the forward on the rectangular problem:
+ *   O_i = sum_j softmax_j(tau q_i . k_j) v_j,  LSE_i = ln sum_j exp(tau q_i . k_j),
+ * over the visible keys j: all Nk, or with causal = 1 (the queries being the
+ * last Nq positions of the sequence) j <= i + Nk - Nq.
+ *
+ * Q, O: bf16 [B,H,Nq,d]; K, V: bf16 [B,H,Nk,d]; LSE: fp32 [B,H,Nq]; all device
+ * pointers, contiguous, 16-byte aligned.  1 <= Nq <= 8 (else
+ * FA_ERR_UNSUPPORTED); Nk >= 1, and Nq <= Nk when causal (else
+ * FA_ERR_INVALID_ARG); d in {64, 128}.  The KV cache is cut into chunks
+ * processed in parallel; their partial results go to `workspace`, which needs
+ * fa_decode_workspace_size(B, H, Nq, Nk, d) bytes (0 when one chunk suffices;
+ * NULL: the call takes it with cudaMallocAsync on `stream` and frees it with
+ * cudaFreeAsync).  Asynchronous on `stream`.
+ */
+FA_API size_t fa_decode_workspace_size(int B, int H, int Nq, int Nk, int d);
+FA_API fa_status fa_fwd_decode(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                               int B, int H, int Nq, int Nk, int d, float tau, int causal,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Kernel timing hook.  With both events non-NULL (cudaEvent_t created by the
  * caller), every later forward or backward call made from the
  * calling host thread records `start` on its stream right before the
