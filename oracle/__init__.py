@@ -13,8 +13,8 @@ Every function takes arrays shaped ``[BH, N, d]`` (or ``[B, H, N, d]``; only
 the trailing two axes matter) in float64, C-contiguous.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``,
-``tests/test_oracle_window_pins.py``, ``tests/test_oracle_blocks_pins.py`` and
-``tests/test_oracle_decode_pins.py``
+``tests/test_oracle_window_pins.py``, ``tests/test_oracle_blocks_pins.py``,
+``tests/test_oracle_decode_pins.py`` and ``tests/test_oracle_fp8_pins.py``
 (closed forms, hand-worked golden values, finite differences, invariants,
 brute force on tiny inputs and an independent transcription of the pages'
 blocked loop).
@@ -101,6 +101,8 @@ def _load():
         lib.ora_attn_bwd_blocks.restype = None
         lib.ora_attn_bwd_blocks.argtypes = [dp, dp, dp, dp, i64, i64, i64, ctypes.c_double, ci,
                                             u8, i64, i64, dp, dp, dp, dp, dp, dp]
+        lib.ora_e4m3_decode.restype = None
+        lib.ora_e4m3_decode.argtypes = [ctypes.c_void_p, i64, dp]
         lib.ora_attn_fwd_decode.restype = None
         lib.ora_attn_fwd_decode.argtypes = [dp, dp, dp, i64, i64, i64, i64, ctypes.c_double,
                                             ctypes.c_int, dp, dp]
@@ -251,6 +253,28 @@ def fwd_decode(q, k, v, tau: float, causal: bool):
     _load().ora_attn_fwd_decode(_ptr(q), _ptr(k), _ptr(v), BH, Nq, Nk, d, float(tau), int(causal),
                                 _ptr(O), _ptr(L))
     return O, L
+
+
+def e4m3_to_f64(x) -> np.ndarray:
+    """Decode e4m3 bytes (uint8 array or tensor, any shape) to float64."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").contiguous().view(-1).numpy().view(np.uint8).reshape(tuple(x.shape))
+    b = np.ascontiguousarray(np.asarray(x), dtype=np.uint8)
+    out = np.empty(b.shape, dtype=np.float64)
+    _load().ora_e4m3_decode(b.ctypes.data, b.size, _ptr(out))
+    return out
+
+
+def fwd_fp8(q8, k8, v8, q_scale: float, k_scale: float, v_scale: float, tau: float,
+            causal: bool, rows=None):
+    """Forward of the FP8 inputs: the plain forward (or its row subset) of the
+    decoded values x * scale."""
+    q = e4m3_to_f64(q8) * float(q_scale)
+    k = e4m3_to_f64(k8) * float(k_scale)
+    v = e4m3_to_f64(v8) * float(v_scale)
+    if rows is None:
+        return fwd(q, k, v, tau, causal)
+    return fwd_rows(q, k, v, tau, causal, rows)
 
 
 def bwd(q, k, v, do, tau: float, causal: bool, want_fwd: bool = False, window=None,

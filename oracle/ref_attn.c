@@ -453,3 +453,27 @@ void ora_attn_fwd_decode(const double* Q, const double* K, const double* V, int6
         free(p);
     }
 }
+
+/*
+ * FP8 inputs.  The FP8 forward of the pages' FlashAttention-3 note ("Atencao
+ * eficiente - FlashAttention, sparse e hibrida", the FlashAttention-4 box)
+ * takes e4m3 tensors with one scale each; the attention it approximates is
+ * the plain definition above on the decoded values x * scale, so the oracle
+ * only adds the decoding.  OCP FP8 E4M3: bit 7 sign, bits 3-6 exponent e
+ * (bias 7), bits 0-2 mantissa m; e = 0 is subnormal, (m / 8) 2^-6; otherwise
+ * (1 + m / 8) 2^(e - 7); e = 15 with m = 7 is NaN; there are no infinities.
+ */
+void ora_e4m3_decode(const uint8_t* x, int64_t n, double* out)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        const int s = x[i] >> 7, e = (x[i] >> 3) & 15, m = x[i] & 7;
+        double v;
+        if (e == 15 && m == 7)
+            v = NAN;
+        else if (e == 0)
+            v = ldexp((double)m / 8.0, -6);
+        else
+            v = ldexp(1.0 + (double)m / 8.0, e - 7);
+        out[i] = s ? -v : v;
+    }
+}

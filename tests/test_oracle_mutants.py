@@ -15,7 +15,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "ref_attn.c")
 PIN_FILES = [os.path.join(ROOT, "tests", f)
              for f in ("test_oracle_pins.py", "test_oracle_window_pins.py", "test_oracle_blocks_pins.py",
-                       "test_oracle_decode_pins.py")]
+                       "test_oracle_decode_pins.py", "test_oracle_fp8_pins.py")]
 
 MUTANTS = {
     "scores_without_tau": ("p[j] = tau * dot(q, K + j * d, d);", "p[j] = dot(q, K + j * d, d);"),
@@ -36,6 +36,9 @@ MUTANTS = {
     "blocks_one_head": ("vs->blocks[bh * vs->head_stride + ", "vs->blocks[0 * vs->head_stride + "),
     "blocks_edge_off_by_one": ("(i / vs->blk) * vs->nkb + j / vs->blk]", "((i + 1) / vs->blk) * vs->nkb + j / vs->blk]"),
     "empty_row_not_guarded": ("    if (seen == 0) {", "    if (seen < 0) {"),
+    "e4m3_bias_off_by_one": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    "e4m3_subnormal_scale": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    "e4m3_mantissa_width": ("ldexp(1.0 + (double)m / 8.0,", "ldexp(1.0 + (double)m / 16.0,"),
     "lse_without_max": ("*lse = m + log(l);", "*lse = log(l);"),
     "no_normalisation": ("for (int64_t j = 0; j < N; ++j) p[j] /= l;", ""),
     "output_wrong_value_row": ("const double* v = V + j * d;", "const double* v = V + (N - 1 - j) * d;"),
