@@ -304,6 +304,8 @@ def run_ours(args):
     blocks_leg = (measure_blocks(w, q, k, v, do, dev, min(args.steps, 20), peak)
                   if args.blocks and w.causal else None)
     decode_leg = measure_decode(dev, min(args.steps, 20), peaks) if args.decode else None
+    fp8_leg = (measure_fp8(w, dev, min(args.steps, 20), peak)
+               if args.fp8 and d == 128 else None)
     e2e = run_e2e(args, w, x, dev, f_step) if not args.no_e2e else None
     cpu = run_cpu_baseline(w, budget_s=args.cpu_seconds) if (rank == 0 and not args.no_cpu) else None
 
@@ -332,6 +334,7 @@ def run_ours(args):
         "sliding_window": window_leg,
         "block_sparse": blocks_leg,
         "decode": decode_leg,
+        "fp8": fp8_leg,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 4 * args.steps,
@@ -476,6 +479,47 @@ def measure_decode(dev, steps, peaks):
             "kernels": "fa_decode_split_kernel" + (" + fa_decode_combine_kernel" if need else "")}
 
 
+def measure_fp8(w, dev, steps, peak_bf16):
+    """FP8 forward (fa_fwd_fp8) on the same shape with seeded e4m3 inputs
+    (per-tensor scale amax / 448): CUDA-event time of the kernel and TFLOP/s on
+    the causal count, against the fp8 peak = measured bf16 peak x 2 (the
+    nominal dense fp8 / bf16 ratio, 4.5 / 2.25 PFLOP/s)."""
+    import torch
+    from exact_io_aware_12_gb300 import api, _lib
+    from exact_io_aware_12_gb300.workloads import draw_fp8, flops_fwd
+
+    B, H, N, d = w.shape
+    x = draw_fp8(B, H, N, d, w.seed)
+    q8, k8, v8 = (x[n].to(dev) for n in ("q8", "k8", "v8"))
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    sc = (x["q_scale"], x["k_scale"], x["v_scale"])
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        api.fwd_fp8(q8, k8, v8, *sc, w.causal, w.tau, out=o, lse=lse)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for e in sum(ev, []):
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        flush.fill_(float(i))
+        _lib.check(_lib.fa_set_timing_events(ev[i][0].cuda_event, ev[i][1].cuda_event), "timing")
+        api.fwd_fp8(q8, k8, v8, *sc, w.causal, w.tau, out=o, lse=lse)
+        _lib.check(_lib.fa_set_timing_events(None, None), "timing")
+    torch.cuda.synchronize(dev)
+    if api.last_device_error(dev) != _lib.FA_OK:
+        raise RuntimeError("kernel watchdog fired in the fp8 leg")
+    ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    ff = flops_fwd(B, H, N, d, w.causal)
+    peak = 2.0 * peak_bf16
+    tf = ff / ms / 1e9
+    return {"steps": steps, "fwd": {"ms": round(ms, 4), "tflops": round(tf, 2),
+                                    "frac": round(tf / peak, 4)},
+            "peak_tflops": peak, "peak_source": "measured bf16 burst x 2 (nominal fp8/bf16 ratio)",
+            "dtype": "e4m3 in, bf16 O"}
+
+
 def run_e2e(args, w, x, dev, f_step):
     """Same step through the public API with host buffers: pinned host inputs
     copied in, outputs (O, LSE, dQ, dK, dV) copied back, inside the timing."""
@@ -615,6 +659,7 @@ def main(argv=None):
                     help="skip the block-sparse leg")
     ap.add_argument("--no-decode", dest="decode", action="store_false",
                     help="skip the decode leg")
+    ap.add_argument("--no-fp8", dest="fp8", action="store_false", help="skip the FP8 leg")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

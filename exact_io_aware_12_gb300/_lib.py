@@ -37,6 +37,7 @@ SIGNATURES = {
     "fa_fwd_window": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_window": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _F, _F, _F, _P]),
     "fa_decode_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "fa_fwd_decode": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     "fa_fwd_blocks": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _I, _P]),
@@ -104,6 +105,11 @@ def fa_bwd_window(Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B
                   window, stream) -> int:
     return _call("fa_bwd_window", Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B,
                  H, N, d, tau, window, stream)
+
+
+def fa_fwd_fp8(Q, K, V, O, LSE, B, H, N, d, tau, causal, q_scale, k_scale, v_scale, stream) -> int:
+    return _call("fa_fwd_fp8", Q, K, V, O, LSE, B, H, N, d, tau, causal, q_scale, k_scale, v_scale,
+                 stream)
 
 
 def fa_decode_workspace_size(B, H, Nq, Nk, d) -> int:

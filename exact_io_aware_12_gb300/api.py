@@ -139,6 +139,31 @@ def bwd(q, k, v, o, do, lse, causal: bool, tau: Optional[float] = None,
     return dq, dk, dv
 
 
+def fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale: float, k_scale: float,
+            v_scale: float, causal: bool, tau: Optional[float] = None,
+            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None):
+    """FP8 forward (fa_fwd_fp8): q8, k8, v8 hold e4m3 bytes (uint8 or
+    float8_e4m3fn tensors, contiguous, [B, H, N, 128]) whose values are
+    byte * scale.  Returns (O bf16 [B, H, N, 128], LSE fp32 [B, H, N])."""
+    ts = (q8, k8, v8)
+    for t in ts:
+        if not t.is_cuda or t.element_size() != 1 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q8, k8, v8 must be contiguous CUDA [B, H, N, d] 1-byte tensors")
+        if t.shape != q8.shape or t.device != q8.device:
+            raise ValueError("q8, k8, v8 must share shape and device")
+    B, H, N, d = q8.shape
+    tau = 1.0 / math.sqrt(d) if tau is None else float(tau)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    code = _lib.fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(),
+                           lse.data_ptr(), B, H, N, d, tau, int(bool(causal)), float(q_scale),
+                           float(k_scale), float(v_scale), _stream_handle(q8.device))
+    _lib.check(code, "fa_fwd_fp8")
+    return out, lse
+
+
 def decode_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
     return _lib.fa_decode_workspace_size(B, H, Nq, Nk, d)
 

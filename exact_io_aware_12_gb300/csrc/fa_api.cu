@@ -429,6 +429,48 @@ fa_status fa_fwd_decode(const void* Q, const void* K, const void* V, void* O, fl
     return map_cuda(e);
 }
 
+fa_status fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                     int N, int d, float tau, int causal, float q_scale, float k_scale,
+                     float v_scale, void* stream) {
+    bool empty = false;
+    fa_status s = check_shape(B, H, N, d, tau, causal, &empty);
+    if (s != FA_OK || empty) return s;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    const float scales[] = {q_scale, k_scale, v_scale};
+    for (float sc : scales)
+        if (!(std::isfinite(sc) && sc > 0.f)) return FA_ERR_INVALID_ARG;
+    const void* ptrs[] = {Q, K, V, O, LSE};
+    for (const void* p : ptrs)
+        if (p == nullptr || !aligned16(p)) return FA_ERR_INVALID_ARG;
+    const size_t rows = static_cast<size_t>(B) * H * N;
+    const size_t in_bytes = rows * d, o_bytes = rows * d * 2, l_bytes = rows * 4;
+    const void* ins[] = {Q, K, V};
+    for (const void* in : ins)
+        if (overlaps(O, o_bytes, in, in_bytes) || overlaps(LSE, l_bytes, in, in_bytes))
+            return FA_ERR_INVALID_ARG;
+    if (overlaps(O, o_bytes, LSE, l_bytes)) return FA_ERR_INVALID_ARG;
+    DeviceInfo* di = current_device(&s);
+    if (!di) return s;
+    Fp8Args a;
+    a.Q = Q;
+    a.K = K;
+    a.V = V;
+    a.O = O;
+    a.LSE = LSE;
+    a.BH = B * H;
+    a.N = N;
+    a.tau = tau;
+    a.q_scale = q_scale;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.causal = causal != 0;
+    a.err = di->err_word;
+    a.wait_limit_ns = g_wait_limit_ns.load();
+    a.ev_start = t_ev_start;
+    a.ev_stop = t_ev_stop;
+    return map_cuda(launch_fwd_fp8(a, static_cast<cudaStream_t>(stream)));
+}
+
 const char* fa_status_string(fa_status s) {
     switch (s) {
         case FA_OK: return "FA_OK";

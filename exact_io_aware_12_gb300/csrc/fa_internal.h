@@ -58,6 +58,23 @@ struct BwdArgs {
     cudaEvent_t ev_stop;
 };
 
+// Arguments of one FP8 (e4m3) forward: Q, K, V are e4m3 bytes [BH][N][128]
+// with one scale per tensor (value = byte * scale); O bf16, LSE fp32.
+struct Fp8Args {
+    const void* Q;
+    const void* K;
+    const void* V;
+    void* O;
+    float* LSE;
+    int BH, N;
+    float tau, q_scale, k_scale, v_scale;
+    bool causal;
+    unsigned int* err;
+    unsigned long long wait_limit_ns;
+    cudaEvent_t ev_start;  // optional: recorded around the kernel
+    cudaEvent_t ev_stop;
+};
+
 // Arguments of one decode forward (split kernel + combine kernel).
 struct DecArgs {
     const void* Q;    // bf16 [BH][Nq][d]
@@ -89,6 +106,7 @@ bool make_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecArgs& a, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const Fp8Args& a, cudaStream_t stream);
 cudaError_t launch_watchdog_selftest(unsigned int* err, unsigned long long limit_ns,
                                      cudaStream_t stream);
 

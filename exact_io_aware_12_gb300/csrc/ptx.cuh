@@ -244,6 +244,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format 0 in bits
+// 7-9 and 10-12) and fp32 accumulation; other fields as idesc_bf16.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4) | (static_cast<uint32_t>(a_mn_major) << 15) |
+           (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // D(tmem) (+)= A(smem desc) * B(smem desc)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -327,6 +335,23 @@ __device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint32_t a_lo, uint
         " mov.b64 db, {%2, %3};\n"
         " elect.sync _|e, 0xffffffff;\n"
         " @e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, %5;\n"
+        "}\n"
+        ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC)
+        : "memory");
+}
+
+// The same for kind::f8f6f4 (8-bit A and B from shared memory, K = 32 per MMA).
+template <int ACC>
+__device__ __forceinline__ void mma_ss_f8_warp(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                               uint32_t hi, uint32_t idesc) {
+    asm volatile(
+        "{\n"
+        " .reg .b64 da, db;\n"
+        " .reg .pred e;\n"
+        " mov.b64 da, {%1, %3};\n"
+        " mov.b64 db, {%2, %3};\n"
+        " elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %4, %5;\n"
         "}\n"
         ::"r"(d_tmem), "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC)
         : "memory");
@@ -463,6 +488,21 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // ----------------------------------------------- paired fp32 arithmetic ----
 // sm_100+ executes one f32x2 instruction for two fp32 lanes held in a 64-bit
 // register pair (element 0 in the low half).
+// Four floats -> four e4m3 bytes (round to nearest even, saturating to +-448),
+// a in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+    uint32_t r;
+    asm("{\n"
+        " .reg .b16 lo, hi;\n"
+        " cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+        " cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+        " mov.b32 %0, {lo, hi};\n"
+        "}\n"
+        : "=r"(r)
+        : "f"(a), "f"(b), "f"(c), "f"(d));
+    return r;
+}
+
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));

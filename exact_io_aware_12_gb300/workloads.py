@@ -186,3 +186,18 @@ def draw_decode(B: int, H: int, Nq: int, Nk: int, d: int, seed: int) -> Dict[str
     k = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32)
     v = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32)
     return {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16)}
+
+
+def draw_fp8(B: int, H: int, N: int, d: int, seed: int) -> Dict[str, object]:
+    """Seeded FP8 inputs: Q, K, V drawn as float32 N(0, 1) (one CPU generator,
+    in that order), each given the per-tensor scale amax / 448 and rounded to
+    e4m3 (torch float8_e4m3fn, round to nearest even).  Returns the e4m3 bytes
+    (uint8 [B, H, N, d]) as q8, k8, v8 and the scales q_scale, k_scale, v_scale."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    out: Dict[str, object] = {}
+    for name in ("q", "k", "v"):
+        x = torch.randn((B, H, N, d), generator=g, dtype=torch.float32)
+        scale = float(x.abs().max()) / 448.0
+        out[name + "8"] = (x / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+        out[name + "_scale"] = scale
+    return out

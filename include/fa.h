@@ -207,6 +207,24 @@ FA_API fa_status fa_fwd_decode(const void* Q, const void* K, const void* V, void
                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * FP8 forward ("Atencao eficiente - FlashAttention, sparse e hibrida", the
+ * FlashAttention-4 note: FlashAttention-3 added FP8 for Hopper).  Q, K, V are
+ * e4m3 (OCP FP8 E4M3: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * no infinities, max 448) stored one byte per element, [B,H,N,d] contiguous,
+ * with one scale per tensor: the value of element x is x * scale.  Computes
+ * the attention of those values, O = softmax(tau (sq Q)(sk K)^T [causal])
+ * (sv V), with both products on FP8 tensor cores; the softmax numerator is
+ * rounded to e4m3 before the second product, which is what limits accuracy
+ * (O agrees with the exact result to about 1e-2 relative; LSE, computed from
+ * the unrounded numerator, to about 1e-3).  O: bf16 [B,H,N,d]; LSE: fp32
+ * [B,H,N], natural log.  d = 128 only (else FA_ERR_UNSUPPORTED); scales finite
+ * and > 0 (else FA_ERR_INVALID_ARG).  Other conventions as fa_fwd.
+ */
+FA_API fa_status fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                            int B, int H, int N, int d, float tau, int causal, float q_scale,
+                            float k_scale, float v_scale, void* stream);
+
+/*
  * Kernel timing hook.  With both events non-NULL (cudaEvent_t created by the
  * caller), every later forward or backward call made from the
  * calling host thread records `start` on its stream right before the
