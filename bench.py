@@ -303,7 +303,9 @@ def run_ours(args):
                   if args.window > 0 and w.causal else None)
     blocks_leg = (measure_blocks(w, q, k, v, do, dev, min(args.steps, 20), peak)
                   if args.blocks and w.causal else None)
-    decode_leg = measure_decode(dev, min(args.steps, 20), peaks) if args.decode else None
+    decode_leg = (measure_decode(dev, min(args.steps, 20), peaks,
+                                 tuple(int(v) for v in args.decode_shape.split(",")))
+                  if args.decode else None)
     fp8_leg = (measure_fp8(w, dev, min(args.steps, 20), peak)
                if args.fp8 and d == 128 else None)
     e2e = run_e2e(args, w, x, dev, f_step) if not args.no_e2e else None
@@ -437,7 +439,7 @@ def measure_blocks(w, q, k, v, do, dev, steps, peak):
             **measure_variant(w, q, k, v, do, dev, steps, peak, ff, blocks=mt)}
 
 
-def measure_decode(dev, steps, peaks):
+def measure_decode(dev, steps, peaks, shape=None):
     """Decode step (fa_fwd_decode: split kernel + combine kernel) on the decode
     workload: CUDA-event time around both kernels, and GB/s of the algorithmic
     bytes (Q, K, V read once; O and LSE written once) against the measured HBM
@@ -447,6 +449,11 @@ def measure_decode(dev, steps, peaks):
     from exact_io_aware_12_gb300.workloads import DECODE_BY_NAME, draw_decode
 
     w = DECODE_BY_NAME["decode_b8h16_nq1_nk32768_d128"]
+    name = w.name
+    if shape is not None and shape != (w.B, w.H, w.Nq, w.Nk, w.d):
+        # a smaller case of the same recipe (profiling)
+        w = type(w)("decode_b%dh%d_nq%d_nk%d_d%d" % shape, *shape, w.causal, w.seed)
+        name = w.name
     x = draw_decode(w.B, w.H, w.Nq, w.Nk, w.d, w.seed)
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     o = torch.empty_like(q)
@@ -473,10 +480,11 @@ def measure_decode(dev, steps, peaks):
     nbytes = 2 * (q.numel() + k.numel() + v.numel() + o.numel()) + 4 * lse.numel()
     gbs = nbytes / (ms / 1e3) / 1e9
     peak = float(peaks["hbm_gbs"])
-    return {"workload": w.name, "steps": steps, "ms": round(ms, 4),
+    return {"workload": name, "steps": steps, "ms": round(ms, 4),
             "bytes": nbytes, "gbs": round(gbs, 1), "peak_gbs": peak,
             "frac": round(gbs / peak, 4), "bound": "hbm",
-            "kernels": "fa_decode_split_kernel" + (" + fa_decode_combine_kernel" if need else "")}
+            "kernels": "fa_decode_split_kernel" + (" + fa_decode_combine_kernel" if need else ""),
+            "traffic": profiled_traffic("decode_split")}
 
 
 def measure_fp8(w, dev, steps, peak_bf16):
@@ -517,7 +525,7 @@ def measure_fp8(w, dev, steps, peak_bf16):
     return {"steps": steps, "fwd": {"ms": round(ms, 4), "tflops": round(tf, 2),
                                     "frac": round(tf / peak, 4)},
             "peak_tflops": peak, "peak_source": "measured bf16 burst x 2 (nominal fp8/bf16 ratio)",
-            "dtype": "e4m3 in, bf16 O"}
+            "dtype": "e4m3 in, bf16 O", "traffic": profiled_traffic("fwd_fp8")}
 
 
 def run_e2e(args, w, x, dev, f_step):
@@ -660,6 +668,8 @@ def main(argv=None):
     ap.add_argument("--no-decode", dest="decode", action="store_false",
                     help="skip the decode leg")
     ap.add_argument("--no-fp8", dest="fp8", action="store_false", help="skip the FP8 leg")
+    ap.add_argument("--decode-shape", default="8,16,1,32768,128",
+                    help="B,H,Nq,Nk,d of the decode leg (a smaller case: profiling only)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
