@@ -268,7 +268,6 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         int qsp = -1;  // block mask: the query tile of the last step
         for (int s = 0; s < n_steps; ++s) {
             const int st = s & 1;
-            if (s >= 2 && !mbar_wait(bar_qe + 8 * st, ((s >> 1) - 1) & 1, wd, kSiteProd)) break;
             int qtile = first + s;
             if constexpr (SPARSE) {
                 qsp = next_set_bit(sh.qbits, nullptr, qsp + 1, n_q);
@@ -276,25 +275,32 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             }
             const int q_start = qtile * kBQ;
             const int64_t row0 = static_cast<int64_t>(bh) * N;
+            // this step's LSE and D into registers first: their latency overlaps
+            // the wait for the stage (stored negated: the softmax warps add them
+            // with paired fp32 ops)
+            float lv[4], dv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int c = lane * 4 + e;
-                const int q = q_start + c;
-                // stored negated: the softmax warps add them with paired fp32 ops
-                lse2_s[st * 128 + c] = q < N ? -p.LSE[row0 + q] * kLog2e : -INFINITY;
-                dvec_s[st * 128 + c] = q < N ? -p.Dvec[row0 + q] : 0.f;
+                const int q = q_start + lane * 4 + e;
+                lv[e] = q < N ? -p.LSE[row0 + q] * kLog2e : -INFINITY;
+                dv[e] = q < N ? -p.Dvec[row0 + q] : 0.f;
             }
+            if (s >= 2 && !mbar_wait(bar_qe + 8 * st, ((s >> 1) - 1) & 1, wd, kSiteProd)) break;
             const uint32_t stage = sbase + L::kStage0 + st * L::kStageBytes;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar_qf + 8 * st, 2 * L::kTile);
+            if (lane == 0) {  // the bulk copies first, then the vectors
+                mbar_expect_tx(bar_qf + 8 * st, 2 * L::kTile);
                 for (int b = 0; b < L::kBoxes; ++b) {
                     tma_load_3d(stage + b * L::kBox, &tmQ, bar_qf + 8 * st, b * 64, q_start, bh);
                     tma_load_3d(stage + L::kTile + b * L::kBox, &tmdO, bar_qf + 8 * st, b * 64,
                                 q_start, bh);
                 }
-            } else {
-                mbar_arrive(bar_qf + 8 * st);
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                lse2_s[st * 128 + lane * 4 + e] = lv[e];
+                dvec_s[st * 128 + lane * 4 + e] = dv[e];
+            }
+            mbar_arrive(bar_qf + 8 * st);  // 32 arrivals; the phase also waits for the copies
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA --
