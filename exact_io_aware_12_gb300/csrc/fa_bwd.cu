@@ -82,6 +82,7 @@ struct BwdBarriers {
     uint64_t dq_full;
     uint64_t dq_drained;
     uint64_t dq_staged;
+    uint64_t dk_done;
     uint32_t tmem_base;
     int abort_flag;
     uint32_t qbits[kMaskWords];  // kMaskBlocks: bit i = this key tile is visited by query tile i
@@ -199,6 +200,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const uint32_t bar_dq = smem_addr(&sh.dq_full);
     const uint32_t bar_dr = smem_addr(&sh.dq_drained);
     const uint32_t bar_sg = smem_addr(&sh.dq_staged);
+    const uint32_t bar_dk = smem_addr(&sh.dk_done);
 
     if (threadIdx.x == 0) {
         sh.abort_flag = 0;
@@ -214,6 +216,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         mbar_init(bar_dq, 1);
         mbar_init(bar_dr, 256);
         mbar_init(bar_sg, 256);
+        mbar_init(bar_dk, 1);
         mbar_init_fence();
     }
     if (warp == kMmaWarp) {
@@ -335,13 +338,16 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 mma_tmem_a<D>(tmem + L::kTmDV, tmem + L::kTmS, do_mn0 + so, s > 0);   // dV
                 if (!__all_sync(0xffffffffu, mbar_wait(bar_ds, s & 1, wd, kSiteMmaDS))) { ok = false; break; }
                 tc_fence_after();
-                mma_tmem_a<D>(tmem + L::kTmDK, tmem + L::kTmDP, q_mn0 + so, s > 0);   // dK
+                // dQ before dK: its drain (and so the next S^T over its columns)
+                // can start while dK runs
                 if (!L::kDQAliasS && s > 0) {
                     if (!__all_sync(0xffffffffu, mbar_wait(bar_dr, (s - 1) & 1, wd, kSiteMmaDrain))) { ok = false; break; }
                     tc_fence_after();
                 }
                 mma_mn_mn<D>(tmem + L::kTmDQ, ds_mn, k_mn);                            // dQ
                 mma_commit_warp(bar_dq);
+                mma_tmem_a<D>(tmem + L::kTmDK, tmem + L::kTmDP, q_mn0 + so, s > 0);   // dK
+                mma_commit_warp(bar_dk);
                 mma_commit_warp(bar_qe + 8 * st);
                 if (s + 1 < n_steps) {
                     const int st1 = (s + 1) & 1;
@@ -504,16 +510,22 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             // dQ drain: this warpgroup's D/2 columns -> fp32 tiles -> bulk reduce-add
             if (ok) ok = __all_sync(FULL, mbar_wait(bar_dq, s & 1, wd, kSiteDrain));
             uint8_t* stage = smem + L::kStage0 + st * L::kStageBytes;
+            uint32_t acc[kDrainBoxes][32];
             if (ok) {
                 tc_fence_after();
-                uint32_t acc[kDrainBoxes][32];
 #pragma unroll
                 for (int b = 0; b < kDrainBoxes; ++b) tmem_ld32(tDQ + 32 * b, acc[b]);
 #pragma unroll
                 for (int b = 0; b < kDrainBoxes; ++b) tmem_ld_wait(acc[b]);
                 tc_fence_before();
                 mbar_arrive(bar_dr);
-                // Q_i + dO_i of this step are free now: stage fp32 boxes of [128 x 32]
+                // stage fp32 boxes of [128 x 32] over this step's Q (warpgroup 0) and dO
+                // (warpgroup 1): dO is free (dV, dP^T done before dQ), Q once dK is
+                if (h == 0) ok = __all_sync(FULL, mbar_wait(bar_dk, s & 1, wd, kSiteDrain));
+            } else {
+                mbar_arrive(bar_dr);
+            }
+            if (ok) {
 #pragma unroll
                 for (int b = 0; b < kDrainBoxes; ++b) {
                     uint8_t* box = stage + (h * kDrainBoxes + b) * L::kBox + r * 128;
@@ -524,8 +536,6 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                                        acc[b][4 * j + 3]);
                 }
                 fence_async_shared();
-            } else {
-                mbar_arrive(bar_dr);
             }
             mbar_arrive(bar_sg);  // the reducer warp adds the staged tiles into dQ
         }
