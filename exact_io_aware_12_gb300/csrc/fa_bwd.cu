@@ -64,7 +64,7 @@ struct BwdLayout {
     static constexpr int kDSBytes = 128 * 128 * 2;
     static constexpr int kVec = kDS + kDSBytes;  // lse2[2][128], dvec[2][128]
     static constexpr int kBars = kVec + 4 * 128 * 4;
-    static constexpr int kBytes = kBars + 256;
+    static constexpr int kBytes = kBars + 512;
     // tensor-memory columns
     static constexpr uint32_t kTmDV = 0, kTmDK = D, kTmS = 2 * D, kTmDP = 2 * D + 128;
     static constexpr bool kDQAliasS = (D == 128);
@@ -73,15 +73,18 @@ struct BwdLayout {
 
 struct BwdBarriers {
     uint64_t kv_full;
-    uint64_t qdo_full[2];
-    uint64_t qdo_empty[2];
+    uint64_t q_full[2];    // Q tile (and the LSE / D vectors) of stage s loaded
+    uint64_t do_full[2];   // dO tile of stage s loaded
+    uint64_t q_empty[2];   // stage s's Q half free: MMAs done, staged dQ half read
+    uint64_t do_empty[2];  // stage s's dO half free: MMAs done, staged dQ half read
     uint64_t s_full;
     uint64_t dp_full;
     uint64_t p_ready;
     uint64_t ds_ready;
     uint64_t dq_full;
     uint64_t dq_drained;
-    uint64_t dq_staged;
+    uint64_t dq_staged_q;   // warpgroup 0 staged its dQ half (over Q)
+    uint64_t dq_staged_do;  // warpgroup 1 staged its dQ half (over dO)
     uint64_t dk_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -191,15 +194,18 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
 
     const uint32_t bar_kv = smem_addr(&sh.kv_full);
-    const uint32_t bar_qf = smem_addr(&sh.qdo_full[0]);
-    const uint32_t bar_qe = smem_addr(&sh.qdo_empty[0]);
+    const uint32_t bar_qf = smem_addr(&sh.q_full[0]);
+    const uint32_t bar_df = smem_addr(&sh.do_full[0]);
+    const uint32_t bar_qe = smem_addr(&sh.q_empty[0]);
+    const uint32_t bar_de = smem_addr(&sh.do_empty[0]);
     const uint32_t bar_s = smem_addr(&sh.s_full);
     const uint32_t bar_dp = smem_addr(&sh.dp_full);
     const uint32_t bar_p = smem_addr(&sh.p_ready);
     const uint32_t bar_ds = smem_addr(&sh.ds_ready);
     const uint32_t bar_dq = smem_addr(&sh.dq_full);
     const uint32_t bar_dr = smem_addr(&sh.dq_drained);
-    const uint32_t bar_sg = smem_addr(&sh.dq_staged);
+    const uint32_t bar_sgq = smem_addr(&sh.dq_staged_q);
+    const uint32_t bar_sgd = smem_addr(&sh.dq_staged_do);
     const uint32_t bar_dk = smem_addr(&sh.dk_done);
 
     if (threadIdx.x == 0) {
@@ -207,7 +213,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         mbar_init(bar_kv, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar_qf + 8 * s, 32);
+            mbar_init(bar_df + 8 * s, 1);
             mbar_init(bar_qe + 8 * s, 2);  // MMA commit + the reducer warp
+            mbar_init(bar_de + 8 * s, 2);
         }
         mbar_init(bar_s, 1);
         mbar_init(bar_dp, 1);
@@ -215,7 +223,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         mbar_init(bar_ds, 256);
         mbar_init(bar_dq, 1);
         mbar_init(bar_dr, 256);
-        mbar_init(bar_sg, 256);
+        mbar_init(bar_sgq, 128);
+        mbar_init(bar_sgd, 128);
         mbar_init(bar_dk, 1);
         mbar_init_fence();
     }
@@ -288,22 +297,28 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 lv[e] = q < N ? -p.LSE[row0 + q] * kLog2e : -INFINITY;
                 dv[e] = q < N ? -p.Dvec[row0 + q] : 0.f;
             }
-            if (s >= 2 && !mbar_wait(bar_qe + 8 * st, ((s >> 1) - 1) & 1, wd, kSiteProd)) break;
+            // the two halves of the stage are refilled as each is freed: dO (whose
+            // staged dQ half is added first), then Q with the vectors
             const uint32_t stage = sbase + L::kStage0 + st * L::kStageBytes;
-            if (lane == 0) {  // the bulk copies first, then the vectors
-                mbar_expect_tx(bar_qf + 8 * st, 2 * L::kTile);
-                for (int b = 0; b < L::kBoxes; ++b) {
-                    tma_load_3d(stage + b * L::kBox, &tmQ, bar_qf + 8 * st, b * 64, q_start, bh);
-                    tma_load_3d(stage + L::kTile + b * L::kBox, &tmdO, bar_qf + 8 * st, b * 64,
+            if (s >= 2 && !mbar_wait(bar_de + 8 * st, ((s >> 1) - 1) & 1, wd, kSiteProd)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar_df + 8 * st, L::kTile);
+                for (int b = 0; b < L::kBoxes; ++b)
+                    tma_load_3d(stage + L::kTile + b * L::kBox, &tmdO, bar_df + 8 * st, b * 64,
                                 q_start, bh);
-                }
+            }
+            if (s >= 2 && !mbar_wait(bar_qe + 8 * st, ((s >> 1) - 1) & 1, wd, kSiteProd)) break;
+            if (lane == 0) {  // the bulk copy first, then the vectors
+                mbar_expect_tx(bar_qf + 8 * st, L::kTile);
+                for (int b = 0; b < L::kBoxes; ++b)
+                    tma_load_3d(stage + b * L::kBox, &tmQ, bar_qf + 8 * st, b * 64, q_start, bh);
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 lse2_s[st * 128 + lane * 4 + e] = lv[e];
                 dvec_s[st * 128 + lane * 4 + e] = dv[e];
             }
-            mbar_arrive(bar_qf + 8 * st);  // 32 arrivals; the phase also waits for the copies
+            mbar_arrive(bar_qf + 8 * st);  // 32 arrivals; the phase also waits for the copy
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA --
@@ -327,8 +342,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 tc_fence_after();
                 mma_rows_rows<D>(tmem + L::kTmS, k_lo, q_lo0);     // S^T
                 mma_commit_warp(bar_s);
-                mma_rows_rows<D>(tmem + L::kTmDP, v_lo, do_lo0);   // dP^T
-                mma_commit_warp(bar_dp);
+                ok = __all_sync(0xffffffffu, mbar_wait(bar_df, 0, wd, kSiteMmaQ));
+                if (ok) {
+                    tc_fence_after();
+                    mma_rows_rows<D>(tmem + L::kTmDP, v_lo, do_lo0);   // dP^T
+                    mma_commit_warp(bar_dp);
+                }
             }
             for (int s = 0; ok && s < n_steps; ++s) {
                 const int st = s & 1;
@@ -336,6 +355,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 if (!__all_sync(0xffffffffu, mbar_wait(bar_p, s & 1, wd, kSiteMmaP))) { ok = false; break; }
                 tc_fence_after();
                 mma_tmem_a<D>(tmem + L::kTmDV, tmem + L::kTmS, do_mn0 + so, s > 0);   // dV
+                mma_commit_warp(bar_de + 8 * st);  // the last MMA that reads this dO
                 if (!__all_sync(0xffffffffu, mbar_wait(bar_ds, s & 1, wd, kSiteMmaDS))) { ok = false; break; }
                 tc_fence_after();
                 // dQ before dK: its drain (and so the next S^T over its columns)
@@ -365,6 +385,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     }
                     mma_rows_rows<D>(tmem + L::kTmS, k_lo, q_lo0 + so1);     // S^T next
                     mma_commit_warp(bar_s);
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_df + 8 * st1, ((s + 1) >> 1) & 1, wd, kSiteMmaQ))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
                     mma_rows_rows<D>(tmem + L::kTmDP, v_lo, do_lo0 + so1);   // dP^T next
                     mma_commit_warp(bar_dp);
                 }
@@ -386,15 +411,25 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     qsp = next_set_bit(sh.qbits, nullptr, qsp + 1, n_q);
                     qtile = qsp;
                 }
-                if (ok) ok = mbar_wait(bar_sg, s & 1, wd, kSiteReduce);
+                const uint32_t src = sbase + L::kStage0 + st * L::kStageBytes;
+                const int q_start = qtile * kBQ;
+                // dQ columns [D/2, D) were staged over dO (warpgroup 1, first),
+                // [0, D/2) over Q (warpgroup 0, once dK is done)
+                if (ok) ok = mbar_wait(bar_sgd, s & 1, wd, kSiteReduce);
                 if (ok) {
-                    const uint32_t src = sbase + L::kStage0 + st * L::kStageBytes;
-                    const int q_start = qtile * kBQ;
-                    for (int b = 0; b < D / 32; ++b)
+                    for (int b = D / 64; b < D / 32; ++b)
                         tma_reduce_add_3d(&tmdQacc, src + b * L::kBox, b * 32, q_start, bh);
                     bulk_commit();
-                    bulk_wait_read<0>();
                 }
+                if (ok) ok = mbar_wait(bar_sgq, s & 1, wd, kSiteReduce);
+                if (ok) {
+                    for (int b = 0; b < D / 64; ++b)
+                        tma_reduce_add_3d(&tmdQacc, src + b * L::kBox, b * 32, q_start, bh);
+                    bulk_commit();
+                    bulk_wait_read<1>();
+                }
+                mbar_arrive(bar_de + 8 * st);
+                if (ok) bulk_wait_read<0>();
                 mbar_arrive(bar_qe + 8 * st);
             }
         }
@@ -537,7 +572,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 }
                 fence_async_shared();
             }
-            mbar_arrive(bar_sg);  // the reducer warp adds the staged tiles into dQ
+            mbar_arrive(h ? bar_sgd : bar_sgq);  // the reducer warp adds the staged tiles into dQ
         }
         // dK = tau * dK_acc and dV (this warpgroup's D/2 columns), staged over the K
         // and V tiles, which no MMA reads any more
