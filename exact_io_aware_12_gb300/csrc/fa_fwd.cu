@@ -37,29 +37,33 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per block
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+// TILES = 2 (the default): two query tiles per CTA, 10 warps, all 512 tensor-
+// memory columns, one CTA per SM.  TILES = 1 (d = 64, short sequences): one
+// tile, 6 warps, 256 columns and a smaller ring, so two CTAs share an SM and
+// one's prologue and epilogue overlap the other's main loop.
+constexpr int threads_for(int tiles) { return tiles == 2 ? 320 : 192; }
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.44269504088896341f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
 // Which keys a query tile visits beyond causality.
 enum : int { kMaskNone = 0, kMaskWindow = 1, kMaskBlocks = 2 };
 constexpr int kMaskWords = kMaxMaskBlocks / 32;
+constexpr int kSingleTileMaxN = 2048;  // d = 64 up to this length: one tile per CTA
 
-template <int D>
+template <int D, int TILES = 2>
 struct FwdLayout {
     static constexpr int kTileBytes = kBM * D * 2;  // one 128-row bf16 tile
     static constexpr int kBoxBytes = 128 * 128;     // one [128 rows x 64 cols] bf16 TMA box
     static constexpr int kBoxes = D / 64;
-    static constexpr int kStages = (D == 64) ? 8 : 4;
+    static constexpr int kStages = TILES == 2 ? ((D == 64) ? 8 : 4) : 5;
     static constexpr int kQ0 = 0;
-    static constexpr int kQ1 = kTileBytes;
-    static constexpr int kRing = 2 * kTileBytes;
+    static constexpr int kQ1 = TILES == 2 ? kTileBytes : 0;
+    static constexpr int kRing = TILES * kTileBytes;
     static constexpr int kBytes = kRing + kStages * kTileBytes;
     static constexpr int kDynSmem = kBytes + 1024;  // + alignment slack
-    static constexpr uint32_t kTmemS0 = 0, kTmemS1 = 128;
-    static constexpr uint32_t kTmemO0 = 256, kTmemO1 = 256 + D;
+    static constexpr uint32_t kTmemS0 = 0, kTmemS1 = TILES == 2 ? 128 : 0;
+    static constexpr uint32_t kTmemO0 = TILES == 2 ? 256 : 128, kTmemO1 = TILES == 2 ? 256 + D : 128;
+    static constexpr uint32_t kTmemCols = TILES == 2 ? 512 : 256;
 };
 
 struct FwdParams {
@@ -125,12 +129,13 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
 
 // MASK: kMaskNone; kMaskWindow, a causal sliding window of p.window keys (only
 // with CAUSAL); kMaskBlocks, the block mask p.blocks (bf16 O only).
-template <int D, bool CAUSAL, bool O32, int MASK>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool CAUSAL, bool O32, int MASK, int TILES>
+__global__ void __launch_bounds__(threads_for(TILES), TILES == 2 ? 1 : 2)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
               const FwdParams p) {
-    using L = FwdLayout<D>;
+    using L = FwdLayout<D, TILES>;
+    constexpr int kProducerWarp = 4 * TILES, kMmaWarp = 4 * TILES + 1;
     constexpr bool LOCAL = MASK == kMaskWindow;
     constexpr bool SPARSE = MASK == kMaskBlocks;
     extern __shared__ uint8_t smem_raw[];
@@ -146,8 +151,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.y);  // heaviest pairs first
     const int N = p.N;
     const int n_kv = (N + kBN - 1) / kBN;
-    const int q_start0 = pair * 2 * kBM;
-    const int q_start1 = q_start0 + kBM;
+    const int q_start0 = pair * TILES * kBM;
+    const int q_start1 = TILES == 2 ? q_start0 + kBM : N;  // TILES = 1: no second tile
     // Key blocks [lo_t, hi_t) of tile t: up to the diagonal when causal, and from
     // the block holding key (first row - window + 1) with a sliding window.  The
     // two ranges overlap or touch, so the loaders walk [jlo, jhi) without gaps.
@@ -183,7 +188,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_init_fence();
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(smem_addr(&sh.tmem_base), 512);
+        tmem_alloc(smem_addr(&sh.tmem_base), L::kTmemCols);
         tmem_relinquish();
     }
     if (warp == kProducerWarp && lane == 0) {
@@ -644,13 +649,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, L::kTmemCols);
     }
 }
 
-template <int D, bool CAUSAL, bool O32, int MASK = kMaskNone>
+template <int D, bool CAUSAL, bool O32, int MASK = kMaskNone, int TILES = 2>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
-    using L = FwdLayout<D>;
+    using L = FwdLayout<D, TILES>;
     CUtensorMap tq, tk, tv, to;
     if (!make_tile_map(&tq, a.Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.BH, 64, kBM) ||
         !make_tile_map(&tk, a.K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.BH, 64, kBN) ||
@@ -661,7 +666,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     } else if (!make_tile_map(&to, a.O, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.BH, 64, kBM)) {
         return cudaErrorInvalidValue;
     }
-    auto kern = fa_fwd_kernel<D, CAUSAL, O32, MASK>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, O32, MASK, TILES>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
     if (e != cudaSuccess) return e;
     FwdParams p;
@@ -671,13 +676,13 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     p.window = (a.window > 0 && a.window < a.N) ? a.window : 0;
     p.blocks = a.blocks;
     p.blocks_head_stride = a.blocks_head_stride;
-    p.n_pairs = (a.N + 2 * kBM - 1) / (2 * kBM);
+    p.n_pairs = (a.N + TILES * kBM - 1) / (TILES * kBM);
     p.scale_log2 = a.tau * kLog2e;
     p.err = a.err;
     p.wait_limit_ns = a.wait_limit_ns;
     dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(p.n_pairs));
     if (a.ev_start) cudaEventRecord(a.ev_start, stream);
-    kern<<<grid, kThreads, L::kDynSmem, stream>>>(tq, tk, tv, to, p);
+    kern<<<grid, threads_for(TILES), L::kDynSmem, stream>>>(tq, tk, tv, to, p);
     e = cudaGetLastError();
     if (e == cudaSuccess && a.ev_stop) e = cudaEventRecord(a.ev_stop, stream);
     return e;
@@ -698,6 +703,9 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
         return a.d == 64 ? launch_fwd_t<64, true, false, kMaskWindow>(a, stream)
                          : launch_fwd_t<128, true, false, kMaskWindow>(a, stream);
     if (a.d == 64) {
+        if (!a.o32 && a.N <= kSingleTileMaxN)
+            return a.causal ? launch_fwd_t<64, true, false, kMaskNone, 1>(a, stream)
+                            : launch_fwd_t<64, false, false, kMaskNone, 1>(a, stream);
         if (a.causal) return a.o32 ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, true, false>(a, stream);
         return a.o32 ? launch_fwd_t<64, false, true>(a, stream) : launch_fwd_t<64, false, false>(a, stream);
     }
