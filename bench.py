@@ -529,8 +529,10 @@ def measure_fp8(w, dev, steps, peak_bf16):
 
 
 def run_e2e(args, w, x, dev, f_step):
-    """Same step through the public API with host buffers: pinned host inputs
-    copied in, outputs (O, LSE, dQ, dK, dV) copied back, inside the timing."""
+    """Same step through the public API with host buffers (api.HostPipeline):
+    every step copies its pinned host inputs in and its outputs (O, LSE, dQ,
+    dK, dV) back, inside the timing; the copies of neighbouring steps overlap
+    the kernels, two device buffer sets deep."""
     import torch
     from exact_io_aware_12_gb300 import api
 
@@ -539,29 +541,26 @@ def run_e2e(args, w, x, dev, f_step):
     hin = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
     dq_, dk_, dv_, o_ = (torch.empty(w.shape, dtype=torch.bfloat16).pin_memory() for _ in range(4))
     lse_ = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    din = {n: torch.empty_like(hin[n], device=dev) for n in hin}
-    ws = torch.empty(api.workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    # the public API's host-buffer pipeline: each step copies its inputs in and
+    # its results out; neighbouring steps' copies overlap each other's kernels
+    pipe = api.HostPipeline(B, H, N, d, w.causal, w.tau, device=dev)
+
     def step():
-        for n in din:
-            din[n].copy_(hin[n], non_blocking=True)
-        o, lse = api.fwd(din["q"], din["k"], din["v"], w.causal, w.tau)
-        dq, dk, dv = api.bwd(din["q"], din["k"], din["v"], o, din["do"], lse, w.causal, w.tau,
-                             workspace=ws)
-        for src, dst in ((o, o_), (lse, lse_), (dq, dq_), (dk, dk_), (dv, dv_)):
-            dst.copy_(src, non_blocking=True)
+        pipe.step(hin["q"], hin["k"], hin["v"], hin["do"], o_, lse_, dq_, dk_, dv_)
 
     for _ in range(max(1, args.warmup)):
         step()
-    torch.cuda.synchronize(dev)
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pipe.synchronize()
     barrier(world, dev)
+    s = torch.cuda.Event(enable_timing=True)
     s.record(stream)
+    pipe.h2d.wait_stream(stream)  # the first timed copy starts after the start event
     for _ in range(args.steps):
         step()
-    e.record(stream)
-    torch.cuda.synchronize(dev)
+    e = pipe.finish_event()
+    e.synchronize()
     t = reduce_max(s.elapsed_time(e) / 1e3, world, dev)
     h2d = sum(t_.numel() * t_.element_size() for t_ in hin.values())
     d2h = sum(t_.numel() * t_.element_size() for t_ in (o_, lse_, dq_, dk_, dv_))

@@ -224,3 +224,70 @@ class _Attention(torch.autograd.Function):
 def attention(q, k, v, causal: bool = False, tau: Optional[float] = None) -> torch.Tensor:
     """O = softmax(tau Q K^T [causal]) V with autograd support."""
     return _Attention.apply(q, k, v, causal, tau)
+
+
+class HostPipeline:
+    """Forward + backward steps on tensors that live in pinned host memory.
+
+    Each step copies its Q, K, V, dO in, runs fwd and bwd, and copies O, LSE,
+    dQ, dK, dV back out.  With ``depth`` device buffer sets (default 2), one
+    stream per copy direction and the compute on the caller's current stream,
+    the copies of neighbouring steps overlap each other's kernels, as a
+    training or serving loop overlaps the next batch's transfer with the
+    current step.  ``step`` only enqueues work; ``synchronize`` waits for all
+    of it.  Host tensors must be pinned, contiguous, of the configured shape
+    (bf16; LSE fp32), and must not be touched until the step has finished."""
+
+    def __init__(self, B: int, H: int, N: int, d: int, causal: bool, tau: Optional[float] = None,
+                 device: Optional[torch.device] = None, depth: int = 2):
+        self.shape = (B, H, N, d)
+        self.causal = bool(causal)
+        self.tau = 1.0 / math.sqrt(d) if tau is None else float(tau)
+        self.device = device or torch.device("cuda", torch.cuda.current_device())
+        self.h2d = torch.cuda.Stream(self.device)
+        self.d2h = torch.cuda.Stream(self.device)
+        ws_bytes = max(workspace_bytes(B, H, N, d), 1)
+        self.bufs = []
+        for _ in range(max(1, depth)):
+            t = {n: torch.empty(self.shape, dtype=torch.bfloat16, device=self.device)
+                 for n in ("q", "k", "v", "do", "o", "dq", "dk", "dv")}
+            t["lse"] = torch.empty((B, H, N), dtype=torch.float32, device=self.device)
+            t["ws"] = torch.empty(ws_bytes, dtype=torch.uint8, device=self.device)
+            t["free"] = torch.cuda.Event()   # outputs copied out: the set may be refilled
+            t["loaded"] = torch.cuda.Event()
+            t["done"] = torch.cuda.Event()
+            self.bufs.append(t)
+        self.k = 0
+
+    def step(self, q, k, v, do, o_out, lse_out, dq_out, dk_out, dv_out) -> None:
+        b = self.bufs[self.k % len(self.bufs)]
+        self.k += 1
+        compute = torch.cuda.current_stream(self.device)
+        with torch.cuda.stream(self.h2d):
+            self.h2d.wait_event(b["free"])
+            for n, src in (("q", q), ("k", k), ("v", v), ("do", do)):
+                b[n].copy_(src, non_blocking=True)
+            b["loaded"].record(self.h2d)
+        compute.wait_event(b["loaded"])
+        fwd(b["q"], b["k"], b["v"], self.causal, self.tau, out=b["o"], lse=b["lse"])
+        bwd(b["q"], b["k"], b["v"], b["o"], b["do"], b["lse"], self.causal, self.tau,
+            dq=b["dq"], dk=b["dk"], dv=b["dv"], workspace=b["ws"])
+        b["done"].record(compute)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(b["done"])
+            for n, dst in (("o", o_out), ("lse", lse_out), ("dq", dq_out), ("dk", dk_out),
+                           ("dv", dv_out)):
+                dst.copy_(b[n], non_blocking=True)
+            b["free"].record(self.d2h)
+
+    def finish_event(self) -> torch.cuda.Event:
+        """An event on the caller's current stream that completes when every
+        step enqueued so far, copies included, has finished."""
+        compute = torch.cuda.current_stream(self.device)
+        compute.wait_stream(self.d2h)
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(compute)
+        return e
+
+    def synchronize(self) -> None:
+        self.finish_event().synchronize()
