@@ -298,7 +298,7 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             l *= alpha;
             const float off = (m_used == -INFINITY) ? 0.f : kShift - m_used;
             const uint64_t c2 = f2_pack(sl2, sl2), o2 = f2_pack(off, off);
-            float ls0 = 0.f, ls1 = 0.f;
+            uint64_t ls2 = 0;  // paired partial sums
             // P (e4m3) to shared memory: 16-byte chunk c of the row holds keys
             // [16c, 16c + 16), placed at chunk c ^ (row & 7) (the 128-byte swizzle)
 #pragma unroll
@@ -312,13 +312,14 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                     const float2 b = f2_unpack(ffma2(
                         f2_pack(u2f(s[k0 >> 5][(k0 & 31) + 2]), u2f(s[k0 >> 5][(k0 & 31) + 3])), c2, o2));
                     const float p0 = ex2(a.x), p1 = ex2(a.y), p2 = ex2(b.x), p3 = ex2(b.y);
-                    ls0 += p0 + p2;
-                    ls1 += p1 + p3;
+                    ls2 = fadd2(ls2, f2_pack(p0, p1));
+                    ls2 = fadd2(ls2, f2_pack(p2, p3));
                     w[q] = pack_e4m3x4(p0, p1, p2, p3);
                 }
                 *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            l += ls0 + ls1;
+            const float2 ls = f2_unpack(ls2);
+            l += ls.x + ls.y;
             fence_async_shared();  // the P V MMA reads P through the async proxy
             if (j > 0 && __any_sync(0xffffffffu, grow)) {
                 // rescale this warp's rows of O once the previous P V has landed
