@@ -38,9 +38,10 @@ namespace {
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per block
 // TILES = 2 (the default): two query tiles per CTA, 10 warps, all 512 tensor-
-// memory columns, one CTA per SM.  TILES = 1 (d = 64, short sequences): one
-// tile, 6 warps, 256 columns and a smaller ring, so two CTAs share an SM and
-// one's prologue and epilogue overlap the other's main loop.
+// memory columns, one CTA per SM.  TILES = 1: one tile, 6 warps, 256 columns
+// and a smaller ring (5 slots at d = 64, 2 at d = 128), so two CTAs share an SM
+// and one's prologue and epilogue overlap the other's main loop: used where a
+// CTA has little work (d = 64 short sequences, block masks).
 constexpr int threads_for(int tiles) { return tiles == 2 ? 320 : 192; }
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.44269504088896341f;
@@ -55,7 +56,7 @@ struct FwdLayout {
     static constexpr int kTileBytes = kBM * D * 2;  // one 128-row bf16 tile
     static constexpr int kBoxBytes = 128 * 128;     // one [128 rows x 64 cols] bf16 TMA box
     static constexpr int kBoxes = D / 64;
-    static constexpr int kStages = TILES == 2 ? ((D == 64) ? 8 : 4) : 5;
+    static constexpr int kStages = TILES == 2 ? ((D == 64) ? 8 : 4) : (D == 64 ? 5 : 2);
     static constexpr int kQ0 = 0;
     static constexpr int kQ1 = TILES == 2 ? kTileBytes : 0;
     static constexpr int kRing = TILES * kTileBytes;
@@ -691,13 +692,13 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
-    if (a.blocks) {
+    if (a.blocks) {  // one tile per CTA: a block mask leaves each CTA little work
         if (a.o32) return cudaErrorInvalidValue;
         if (a.d == 64)
-            return a.causal ? launch_fwd_t<64, true, false, kMaskBlocks>(a, stream)
-                            : launch_fwd_t<64, false, false, kMaskBlocks>(a, stream);
-        return a.causal ? launch_fwd_t<128, true, false, kMaskBlocks>(a, stream)
-                        : launch_fwd_t<128, false, false, kMaskBlocks>(a, stream);
+            return a.causal ? launch_fwd_t<64, true, false, kMaskBlocks, 1>(a, stream)
+                            : launch_fwd_t<64, false, false, kMaskBlocks, 1>(a, stream);
+        return a.causal ? launch_fwd_t<128, true, false, kMaskBlocks, 1>(a, stream)
+                        : launch_fwd_t<128, false, false, kMaskBlocks, 1>(a, stream);
     }
     if (a.causal && !a.o32 && a.window > 0 && a.window < a.N)
         return a.d == 64 ? launch_fwd_t<64, true, false, kMaskWindow>(a, stream)
