@@ -22,6 +22,11 @@
 //     weights sit 2^6 further above e4m3's subnormal range than with P <= 1;
 //     l sums the same (unrounded) P in fp32, so the shift cancels in O / l and
 //     LSE = m - 6 + log2 l (in log2 units, converted at the store);
+//   - P in shared memory frees S's tensor-memory columns as soon as the softmax
+//     has read them, so the MMA warp runs one block ahead: S_t(j+1) is issued
+//     while the softmax still works on block j, and P_t(j) V(j) when its P is
+//     stored; the softmax waits for the previous P V only before overwriting
+//     P's tile (and rescaling O);
 //   - warps 0-3 / 4-7: softmax of query tile 0 / 1; warp 8: TMA; warp 9: MMA.
 #include <cuda_bf16.h>
 
@@ -68,6 +73,7 @@ struct Fp8Shared {
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t s_full[2];
+    uint64_t s_free[2];   // the softmax has read S_t: its columns may be overwritten
     uint64_t p_ready[2];
     uint64_t o_done[2];
     uint32_t tmem_base;
@@ -132,6 +138,7 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     const uint32_t bar_kv_full = smem_addr(&sh.kv_full[0]);
     const uint32_t bar_kv_empty = smem_addr(&sh.kv_empty[0]);
     const uint32_t bar_s = smem_addr(&sh.s_full[0]);
+    const uint32_t bar_sf = smem_addr(&sh.s_free[0]);
     const uint32_t bar_p = smem_addr(&sh.p_ready[0]);
     const uint32_t bar_o = smem_addr(&sh.o_done[0]);
 
@@ -144,6 +151,7 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar_s + 8 * t, 1);
+            mbar_init(bar_sf + 8 * t, 128);
             mbar_init(bar_p + 8 * t, 128);
             mbar_init(bar_o + 8 * t, 1);
         }
@@ -171,14 +179,17 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             mbar_arrive_expect_tx(bar_q, kTile * (1 + (n_blk1 > 0)));
             tma_load_3d(sbase + kQ0, &tmQ, bar_q, 0, q_start0, bh);
             if (n_blk1 > 0) tma_load_3d(sbase + kQ1, &tmQ, bar_q, 0, q_start1, bh);
+            // load order = the MMA warp's use order: K0, K1, V0, K2, V1, ..., V(nb-1)
             for (int ld = 0; ld < 2 * nb; ++ld) {
                 const int slot = ld % kStages;
                 if (ld >= kStages &&
                     !mbar_wait(bar_kv_empty + 8 * slot, ((ld / kStages) - 1) & 1, wd, kSiteProdEmpty))
                     break;
+                const bool is_k = ld == 0 || ((ld & 1) && ld < 2 * nb - 1);
+                const int blk = is_k ? (ld + 1) / 2 : (ld == 2 * nb - 1 ? nb - 1 : ld / 2 - 1);
                 mbar_arrive_expect_tx(bar_kv_full + 8 * slot, kTile);
-                tma_load_3d(sbase + kRing + slot * kTile, (ld & 1) ? &tmV : &tmK,
-                            bar_kv_full + 8 * slot, 0, (ld >> 1) * kBN, bh);
+                tma_load_3d(sbase + kRing + slot * kTile, is_k ? &tmK : &tmV,
+                            bar_kv_full + 8 * slot, 0, blk * kBN, bh);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -191,55 +202,51 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const uint32_t vlo0 = sw128_desc_lo(sbase + kRing, 128 * 128);  // V: MN-major
         constexpr uint32_t kSlot = kTile >> 4;
         const int nblk[2] = {n_blk0, n_blk1};
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteMmaQ) &&
-                                              mbar_wait(bar_kv_full, 0, wd, kSiteMmaKV));
-        if (ok) {
-            tc_fence_after();
-            for (int t = 0; t < 2; ++t) {
-                if (nblk[t] > 0) {
-                    issue_s(tS[t], qlo[t], klo0);
-                    mma_commit_warp(bar_s + 8 * t);
-                }
-            }
-            mma_commit_warp(bar_kv_empty);
-        }
-        for (int j = 0; ok && j < nb; ++j) {
-            const int lv = 2 * j + 1, lk = 2 * j + 2;
-            const int sv = lv % kStages, sk = lk % kStages;
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait(bar_kv_full + 8 * sv, (lv / kStages) & 1, wd, kSiteMmaKV))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            bool k_ready = false;
-            for (int t = 0; t < 2 && ok; ++t) {
-                if (j >= nblk[t]) continue;
-                if (!__all_sync(0xffffffffu, mbar_wait(bar_p + 8 * t, j & 1, wd, kSiteMmaP))) {
+        // Software-pipelined: P lives in shared memory, so S_t(j) needs only the
+        // softmax to have read S_t(j-1) (s_free), not P_t(j-1) V(j-1); iteration j
+        // issues S(j) for both tiles, then P(j-1) V(j-1).
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteMmaQ));
+        for (int j = 0; ok && j <= nb; ++j) {
+            if (j < nb) {
+                const int lk = j == 0 ? 0 : 2 * j - 1, sk = lk % kStages;  // K_j's load index
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(bar_kv_full + 8 * sk, (lk / kStages) & 1, wd, kSiteMmaKV))) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
-                issue_pv(tO[t], plo[t], vlo0 + sv * kSlot, j > 0);
-                mma_commit_warp(bar_o + 8 * t);
-                if (j + 1 < nblk[t]) {
-                    if (!k_ready) {
-                        if (!__all_sync(0xffffffffu,
-                                        mbar_wait(bar_kv_full + 8 * sk, (lk / kStages) & 1, wd,
-                                                  kSiteMmaKV))) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        k_ready = true;
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= nblk[t]) continue;
+                    if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(bar_sf + 8 * t, (j - 1) & 1, wd, kSiteMmaP))) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
                     issue_s(tS[t], qlo[t], klo0 + sk * kSlot);
                     mma_commit_warp(bar_s + 8 * t);
                 }
+                if (!ok) break;
+                mma_commit_warp(bar_kv_empty + 8 * sk);
             }
-            if (!ok) break;
-            mma_commit_warp(bar_kv_empty + 8 * sv);
-            if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
+            if (j > 0) {
+                const int lv = min(2 * (j - 1) + 2, 2 * nb - 1), sv = lv % kStages;  // V_(j-1)'s
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(bar_kv_full + 8 * sv, (lv / kStages) & 1, wd, kSiteMmaKV))) {
+                    ok = false;
+                    break;
+                }
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j - 1 >= nblk[t]) continue;
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_p + 8 * t, (j - 1) & 1, wd, kSiteMmaP))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_pv(tO[t], plo[t], vlo0 + sv * kSlot, j > 1);
+                    mma_commit_warp(bar_o + 8 * t);
+                }
+                if (!ok) break;
+                mma_commit_warp(bar_kv_empty + 8 * sv);
+            }
         }
         __syncwarp();
     } else {
@@ -254,6 +261,7 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const uint32_t tO = tmem + lane_off + (t ? kTmemO1 : kTmemO0);
         uint8_t* prow = smem + (t ? kP1 : kP0) + r * 128;  // this row of P (e4m3, swizzled)
         const uint32_t my_s = bar_s + 8 * t, my_p = bar_p + 8 * t, my_o = bar_o + 8 * t;
+        const uint32_t my_sf = bar_sf + 8 * t;
         const float sl2 = p.scale_log2;
         float m_used = -INFINITY;
         float l = 0.f;
@@ -273,6 +281,8 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             tmem_ld_wait(s[1]);
             tmem_ld_wait(s[2]);
             tmem_ld_wait(s[3]);
+            tc_fence_before();
+            mbar_arrive(my_sf);  // S_t's columns may take the next block's scores now
             const int kbase = j * kBN;
             if ((CAUSAL && kbase + kBN - 1 > q_start) || (kbase + kBN > N)) {
                 const int last = CAUSAL ? min(row, N - 1) : N - 1;  // last visible key
@@ -299,11 +309,11 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             const float off = (m_used == -INFINITY) ? 0.f : kShift - m_used;
             const uint64_t c2 = f2_pack(sl2, sl2), o2 = f2_pack(off, off);
             uint64_t ls2 = 0;  // paired partial sums
-            // P (e4m3) to shared memory: 16-byte chunk c of the row holds keys
-            // [16c, 16c + 16), placed at chunk c ^ (row & 7) (the 128-byte swizzle)
+            // P (e4m3) for the whole row in registers first: its shared-memory tile
+            // is still the A operand of the previous block's P V
+            uint32_t w[8][4];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                uint32_t w[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int k0 = 16 * c + 4 * q;
@@ -314,20 +324,28 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                     const float p0 = ex2(a.x), p1 = ex2(a.y), p2 = ex2(b.x), p3 = ex2(b.y);
                     ls2 = fadd2(ls2, f2_pack(p0, p1));
                     ls2 = fadd2(ls2, f2_pack(p2, p3));
-                    w[q] = pack_e4m3x4(p0, p1, p2, p3);
+                    w[c][q] = pack_e4m3x4(p0, p1, p2, p3);
                 }
-                *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
             const float2 ls = f2_unpack(ls2);
             l += ls.x + ls.y;
-            fence_async_shared();  // the P V MMA reads P through the async proxy
-            if (j > 0 && __any_sync(0xffffffffu, grow)) {
-                // rescale this warp's rows of O once the previous P V has landed
+            if (j > 0) {
+                // the previous P V is done: P's tile is free and O holds blocks < j
                 if (!__all_sync(0xffffffffu, mbar_wait(my_o, (j - 1) & 1, wd, kSiteSoftO))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+            }
+            // 16-byte chunk c of the row holds keys [16c, 16c + 16), placed at chunk
+            // c ^ (row & 7) (the 128-byte swizzle)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
+                    make_uint4(w[c][0], w[c][1], w[c][2], w[c][3]);
+            fence_async_shared();  // the P V MMA reads P through the async proxy
+            if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                // rescale this warp's rows of O (the previous P V has landed)
 #pragma unroll
                 for (int c0 = 0; c0 < kD; c0 += 32) {
                     uint32_t o[32];
