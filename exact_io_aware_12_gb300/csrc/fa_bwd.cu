@@ -465,8 +465,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                                               mbar_wait(bar_qf + 8 * st, (s >> 1) & 1, wd, kSiteDsQ));
             if (ok) {
                 tc_fence_after();
-                // -log2(e) LSE per query, pairs of adjacent queries as one 64-bit value
-                const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(lse2_s + st * 128 + 64 * h);
+                // -log2(e) LSE per query, pairs of adjacent queries as one 64-bit value,
+                // read four queries per 16-byte broadcast load
+                const ulonglong2* nl4 = reinterpret_cast<const ulonglong2*>(lse2_s + st * 128 + 64 * h);
                 const bool diag = CAUSAL && (q_start == kv_start);
                 // window edge: query q no longer sees key kg once q >= kg + window
                 const bool wedge = window > 0 && q_start + kBQ - 1 >= kv_start + window;
@@ -478,11 +479,15 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     tmem_ld32(tS + 32 * c, sv);
                     tmem_ld_wait(sv);
                     uint32_t pk[16];
+                    ulonglong2 nl[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) nl[i] = nl4[8 * c + i];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int q = 32 * c + 2 * i;
+                        const uint64_t nlq = (i & 1) ? nl[i >> 1].y : nl[i >> 1].x;
                         const float2 x = f2_unpack(
-                            ffma2(f2_pack(u2f(sv[2 * i]), u2f(sv[2 * i + 1])), c2, nl2[q >> 1]));
+                            ffma2(f2_pack(u2f(sv[2 * i]), u2f(sv[2 * i + 1])), c2, nlq));
                         float p0 = ex2(x.x);
                         float p1 = ex2(x.y);
                         if (diag) {
@@ -510,8 +515,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                                               (s == 0 || mbar_wait(bar_dq, (s - 1) & 1, wd, kSiteDsDQ)));
             if (ok) {
                 tc_fence_after();
-                // -D per query, pairs of adjacent queries as one 64-bit value
-                const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(dvec_s + st * 128 + 64 * h);
+                // -D per query, pairs of adjacent queries as one 64-bit value (16-byte loads)
+                const ulonglong2* nd4 = reinterpret_cast<const ulonglong2*>(dvec_s + st * 128 + 64 * h);
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t dp[32], pk[16];
@@ -520,11 +525,14 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     tmem_ld_wait(dp);
                     tmem_ld_wait(pk);
                     uint32_t ds[16];
+                    ulonglong2 nd[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) nd[i] = nd4[8 * c + i];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const int q = 32 * c + 2 * i;
+                        const uint64_t ndq = (i & 1) ? nd[i >> 1].y : nd[i >> 1].x;
                         const uint64_t pp = f2_pack(u2f(pk[i] << 16), u2f(pk[i] & 0xffff0000u));
-                        const uint64_t t = fadd2(f2_pack(u2f(dp[2 * i]), u2f(dp[2 * i + 1])), nd2[q >> 1]);
+                        const uint64_t t = fadd2(f2_pack(u2f(dp[2 * i]), u2f(dp[2 * i + 1])), ndq);
                         const float2 d = f2_unpack(fmul2(pp, t));
                         ds[i] = pack_bf16(d.x, d.y);
                     }
