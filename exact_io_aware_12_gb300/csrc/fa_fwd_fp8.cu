@@ -13,20 +13,19 @@
 //     twice the bf16 rate); Q, K and V tiles are [128 x 128 bytes], one
 //     128-byte-swizzled TMA box each, so a K or V slot is 16 KB and the ring
 //     holds 8 of them;
-//   - an MMA takes both operands of one type, so P cannot stay in tensor
-//     memory as bf16: each softmax thread converts its row of P to e4m3
-//     (cvt.rn.satfinite.e4m3x2) and stores it, swizzled, to a shared-memory
-//     tile that the P V product reads as its K-major A operand;
+//   - an MMA takes both operands of one type, so P goes back to tensor memory
+//     as e4m3, not bf16: each softmax thread converts its row of P
+//     (cvt.rn.satfinite.e4m3x2), packs four keys per 32-bit column and writes
+//     the 32 columns over its tile's S, where the P V product reads it as the
+//     A operand (A from tensor memory, V from shared memory).  With P in shared
+//     memory instead, every MMA of the loop reads both operands from shared
+//     memory, which then carries about 1.5 times the MMAs' own cycles per
+//     block and slows them down;
 //   - P = 2^(x - m + 6) with the row max m rescaled only when it grows by more
 //     than 2^2: P stays <= 2^8 (e4m3 saturates at 448) and the smallest
 //     weights sit 2^6 further above e4m3's subnormal range than with P <= 1;
 //     l sums the same (unrounded) P in fp32, so the shift cancels in O / l and
 //     LSE = m - 6 + log2 l (in log2 units, converted at the store);
-//   - P in shared memory frees S's tensor-memory columns as soon as the softmax
-//     has read them, so the MMA warp runs one block ahead: S_t(j+1) is issued
-//     while the softmax still works on block j, and P_t(j) V(j) when its P is
-//     stored; the softmax waits for the previous P V only before overwriting
-//     P's tile (and rescaling O);
 //   - warps 0-3 / 4-7: softmax of query tile 0 / 1; warp 8: TMA; warp 9: MMA.
 #include <cuda_bf16.h>
 
@@ -46,9 +45,10 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTile = kBM * kD;  // one fp8 [128 x 128] tile
 constexpr int kStages = 8;
-// shared memory: [Q0][P0][Q1][P1] (Q_t and P_t adjacent: 32 KB that the bf16 O
-// tile reuses at the end), then the ring of K and V slots
-constexpr int kQ0 = 0, kP0 = kTile, kQ1 = 2 * kTile, kP1 = 3 * kTile, kRing = 4 * kTile;
+// shared memory: [Q0][pad][Q1][pad] (each Q tile followed by 16 KB, so the bf16
+// O tile of 32 KB can be staged over it at the end), then the ring of K and V
+// slots
+constexpr int kQ0 = 0, kQ1 = 2 * kTile, kRing = 4 * kTile;
 constexpr int kBytes = kRing + kStages * kTile;
 constexpr int kDynSmem = kBytes + 1024;  // + alignment slack
 constexpr int kOutBox = 128 * 128;       // one bf16 [128 rows x 64 cols] TMA box of O
@@ -73,7 +73,6 @@ struct Fp8Shared {
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t s_full[2];
-    uint64_t s_free[2];   // the softmax has read S_t: its columns may be overwritten
     uint64_t p_ready[2];
     uint64_t o_done[2];
     uint32_t tmem_base;
@@ -98,16 +97,17 @@ __device__ __forceinline__ void issue_s(uint32_t tmem_d, uint32_t q_lo, uint32_t
     for (int k = 1; k < kD / 32; ++k) mma_ss_f8_warp<1>(tmem_d, q_lo + 2 * k, k_lo + 2 * k, kDescHi, id);
 }
 
-// O += P V: P K-major [128 rows x 128 keys], V MN-major [128 keys x 128 dims];
-// a K-step of 32 keys is 32 rows of V (4 KB).
-__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t p_lo, uint32_t v_lo,
+// O += P V: P [128 rows x 128 keys] e4m3 in tensor memory (four keys per
+// column), V MN-major [128 keys x 128 dims]; a K-step of 32 keys is 8 columns
+// of P and 32 rows of V (4 KB).
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_lo,
                                          bool accumulate) {
     constexpr uint32_t id = idesc_e4m3(128, 128, false, true);
-    if (accumulate) mma_ss_f8_warp<1>(tmem_o, p_lo, v_lo, kDescHi, id);
-    else mma_ss_f8_warp<0>(tmem_o, p_lo, v_lo, kDescHi, id);
+    if (accumulate) mma_ts_f8_warp<1>(tmem_o, tmem_p, v_lo, kDescHi, id);
+    else mma_ts_f8_warp<0>(tmem_o, tmem_p, v_lo, kDescHi, id);
 #pragma unroll
     for (int k = 1; k < kBN / 32; ++k)
-        mma_ss_f8_warp<1>(tmem_o, p_lo + 2 * k, v_lo + ((k * 32 * 128) >> 4), kDescHi, id);
+        mma_ts_f8_warp<1>(tmem_o, tmem_p + 8 * k, v_lo + ((k * 32 * 128) >> 4), kDescHi, id);
 }
 
 template <bool CAUSAL>
@@ -138,7 +138,6 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
     const uint32_t bar_kv_full = smem_addr(&sh.kv_full[0]);
     const uint32_t bar_kv_empty = smem_addr(&sh.kv_empty[0]);
     const uint32_t bar_s = smem_addr(&sh.s_full[0]);
-    const uint32_t bar_sf = smem_addr(&sh.s_free[0]);
     const uint32_t bar_p = smem_addr(&sh.p_ready[0]);
     const uint32_t bar_o = smem_addr(&sh.o_done[0]);
 
@@ -151,7 +150,6 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar_s + 8 * t, 1);
-            mbar_init(bar_sf + 8 * t, 128);
             mbar_init(bar_p + 8 * t, 128);
             mbar_init(bar_o + 8 * t, 1);
         }
@@ -179,17 +177,14 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             mbar_arrive_expect_tx(bar_q, kTile * (1 + (n_blk1 > 0)));
             tma_load_3d(sbase + kQ0, &tmQ, bar_q, 0, q_start0, bh);
             if (n_blk1 > 0) tma_load_3d(sbase + kQ1, &tmQ, bar_q, 0, q_start1, bh);
-            // load order = the MMA warp's use order: K0, K1, V0, K2, V1, ..., V(nb-1)
             for (int ld = 0; ld < 2 * nb; ++ld) {
                 const int slot = ld % kStages;
                 if (ld >= kStages &&
                     !mbar_wait(bar_kv_empty + 8 * slot, ((ld / kStages) - 1) & 1, wd, kSiteProdEmpty))
                     break;
-                const bool is_k = ld == 0 || ((ld & 1) && ld < 2 * nb - 1);
-                const int blk = is_k ? (ld + 1) / 2 : (ld == 2 * nb - 1 ? nb - 1 : ld / 2 - 1);
                 mbar_arrive_expect_tx(bar_kv_full + 8 * slot, kTile);
-                tma_load_3d(sbase + kRing + slot * kTile, is_k ? &tmK : &tmV,
-                            bar_kv_full + 8 * slot, 0, blk * kBN, bh);
+                tma_load_3d(sbase + kRing + slot * kTile, (ld & 1) ? &tmV : &tmK,
+                            bar_kv_full + 8 * slot, 0, (ld >> 1) * kBN, bh);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -197,56 +192,59 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const uint32_t tS[2] = {tmem + kTmemS0, tmem + kTmemS1};
         const uint32_t tO[2] = {tmem + kTmemO0, tmem + kTmemO1};
         const uint32_t qlo[2] = {sw128_desc_lo(sbase + kQ0, 16), sw128_desc_lo(sbase + kQ1, 16)};
-        const uint32_t plo[2] = {sw128_desc_lo(sbase + kP0, 16), sw128_desc_lo(sbase + kP1, 16)};
         const uint32_t klo0 = sw128_desc_lo(sbase + kRing, 16);         // K: K-major
         const uint32_t vlo0 = sw128_desc_lo(sbase + kRing, 128 * 128);  // V: MN-major
         constexpr uint32_t kSlot = kTile >> 4;
         const int nblk[2] = {n_blk0, n_blk1};
-        // Software-pipelined: P lives in shared memory, so S_t(j) needs only the
-        // softmax to have read S_t(j-1) (s_free), not P_t(j-1) V(j-1); iteration j
-        // issues S(j) for both tiles, then P(j-1) V(j-1).
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteMmaQ));
-        for (int j = 0; ok && j <= nb; ++j) {
-            if (j < nb) {
-                const int lk = j == 0 ? 0 : 2 * j - 1, sk = lk % kStages;  // K_j's load index
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(bar_kv_full + 8 * sk, (lk / kStages) & 1, wd, kSiteMmaKV))) {
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteMmaQ) &&
+                                              mbar_wait(bar_kv_full, 0, wd, kSiteMmaKV));
+        if (ok) {
+            tc_fence_after();
+            for (int t = 0; t < 2; ++t) {
+                if (nblk[t] > 0) {
+                    issue_s(tS[t], qlo[t], klo0);
+                    mma_commit_warp(bar_s + 8 * t);
+                }
+            }
+            mma_commit_warp(bar_kv_empty);
+        }
+        for (int j = 0; ok && j < nb; ++j) {
+            const int lv = 2 * j + 1, lk = 2 * j + 2;
+            const int sv = lv % kStages, sk = lk % kStages;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(bar_kv_full + 8 * sv, (lv / kStages) & 1, wd, kSiteMmaKV))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            bool k_ready = false;
+            for (int t = 0; t < 2 && ok; ++t) {
+                if (j >= nblk[t]) continue;
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_p + 8 * t, j & 1, wd, kSiteMmaP))) {
                     ok = false;
                     break;
                 }
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j >= nblk[t]) continue;
-                    if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(bar_sf + 8 * t, (j - 1) & 1, wd, kSiteMmaP))) {
-                        ok = false;
-                        break;
+                tc_fence_after();
+                issue_pv(tO[t], tS[t], vlo0 + sv * kSlot, j > 0);
+                mma_commit_warp(bar_o + 8 * t);
+                if (j + 1 < nblk[t]) {
+                    if (!k_ready) {
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait(bar_kv_full + 8 * sk, (lk / kStages) & 1, wd,
+                                                  kSiteMmaKV))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        k_ready = true;
                     }
-                    tc_fence_after();
                     issue_s(tS[t], qlo[t], klo0 + sk * kSlot);
                     mma_commit_warp(bar_s + 8 * t);
                 }
-                if (!ok) break;
-                mma_commit_warp(bar_kv_empty + 8 * sk);
             }
-            if (j > 0) {
-                const int lv = min(2 * (j - 1) + 2, 2 * nb - 1), sv = lv % kStages;  // V_(j-1)'s
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(bar_kv_full + 8 * sv, (lv / kStages) & 1, wd, kSiteMmaKV))) {
-                    ok = false;
-                    break;
-                }
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j - 1 >= nblk[t]) continue;
-                    if (!__all_sync(0xffffffffu, mbar_wait(bar_p + 8 * t, (j - 1) & 1, wd, kSiteMmaP))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    issue_pv(tO[t], plo[t], vlo0 + sv * kSlot, j > 1);
-                    mma_commit_warp(bar_o + 8 * t);
-                }
-                if (!ok) break;
-                mma_commit_warp(bar_kv_empty + 8 * sv);
-            }
+            if (!ok) break;
+            mma_commit_warp(bar_kv_empty + 8 * sv);
+            if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
         }
         __syncwarp();
     } else {
@@ -259,9 +257,7 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_off + (t ? kTmemS1 : kTmemS0);
         const uint32_t tO = tmem + lane_off + (t ? kTmemO1 : kTmemO0);
-        uint8_t* prow = smem + (t ? kP1 : kP0) + r * 128;  // this row of P (e4m3, swizzled)
         const uint32_t my_s = bar_s + 8 * t, my_p = bar_p + 8 * t, my_o = bar_o + 8 * t;
-        const uint32_t my_sf = bar_sf + 8 * t;
         const float sl2 = p.scale_log2;
         float m_used = -INFINITY;
         float l = 0.f;
@@ -281,8 +277,6 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             tmem_ld_wait(s[1]);
             tmem_ld_wait(s[2]);
             tmem_ld_wait(s[3]);
-            tc_fence_before();
-            mbar_arrive(my_sf);  // S_t's columns may take the next block's scores now
             const int kbase = j * kBN;
             if ((CAUSAL && kbase + kBN - 1 > q_start) || (kbase + kBN > N)) {
                 const int last = CAUSAL ? min(row, N - 1) : N - 1;  // last visible key
@@ -309,9 +303,10 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
             const float off = (m_used == -INFINITY) ? 0.f : kShift - m_used;
             const uint64_t c2 = f2_pack(sl2, sl2), o2 = f2_pack(off, off);
             uint64_t ls2 = 0;  // paired partial sums
-            // P (e4m3) for the whole row in registers first: its shared-memory tile
-            // is still the A operand of the previous block's P V
-            uint32_t w[8][4];
+            // P (e4m3), keys [4i, 4i + 4) in column i of this row, over S: the P V
+            // of the previous block, which read these columns, finished before S
+            // of this block (issued after it) did
+            uint32_t w[32];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
 #pragma unroll
@@ -324,28 +319,19 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                     const float p0 = ex2(a.x), p1 = ex2(a.y), p2 = ex2(b.x), p3 = ex2(b.y);
                     ls2 = fadd2(ls2, f2_pack(p0, p1));
                     ls2 = fadd2(ls2, f2_pack(p2, p3));
-                    w[c][q] = pack_e4m3x4(p0, p1, p2, p3);
+                    w[4 * c + q] = pack_e4m3x4(p0, p1, p2, p3);
                 }
             }
+            tmem_st32(tS, w);
             const float2 ls = f2_unpack(ls2);
             l += ls.x + ls.y;
-            if (j > 0) {
-                // the previous P V is done: P's tile is free and O holds blocks < j
+            if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                // rescale this warp's rows of O once the previous P V has landed
                 if (!__all_sync(0xffffffffu, mbar_wait(my_o, (j - 1) & 1, wd, kSiteSoftO))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-            }
-            // 16-byte chunk c of the row holds keys [16c, 16c + 16), placed at chunk
-            // c ^ (row & 7) (the 128-byte swizzle)
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
-                    make_uint4(w[c][0], w[c][1], w[c][2], w[c][3]);
-            fence_async_shared();  // the P V MMA reads P through the async proxy
-            if (j > 0 && __any_sync(0xffffffffu, grow)) {
-                // rescale this warp's rows of O (the previous P V has landed)
 #pragma unroll
                 for (int c0 = 0; c0 < kD; c0 += 32) {
                     uint32_t o[32];
@@ -355,8 +341,8 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
                     for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
                     tmem_st32(tO + c0, o);
                 }
-                tmem_st_wait();
             }
+            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(my_p);
         }

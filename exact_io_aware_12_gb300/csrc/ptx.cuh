@@ -363,6 +363,22 @@ __device__ __forceinline__ void mma_ss_f8_warp(uint32_t d_tmem, uint32_t a_lo, u
         : "memory");
 }
 
+// D(tmem) (+)= A(tmem, e4m3 four per column) * B(smem desc, e4m3)
+template <int ACC>
+__device__ __forceinline__ void mma_ts_f8_warp(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                               uint32_t hi, uint32_t idesc) {
+    asm volatile(
+        "{\n"
+        " .reg .b64 db;\n"
+        " .reg .pred e;\n"
+        " mov.b64 db, {%2, %3};\n"
+        " elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], db, %4, %5;\n"
+        "}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC)
+        : "memory");
+}
+
 template <int ACC>
 __device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
                                             uint32_t idesc) {
