@@ -583,7 +583,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             mbar_arrive(h ? bar_sgd : bar_sgq);  // the reducer warp adds the staged tiles into dQ
         }
         // dK = tau * dK_acc and dV (this warpgroup's D/2 columns), staged over the K
-        // and V tiles, which no MMA reads any more
+        // and V tiles, which no MMA reads any more: the commit after the last dK
+        // covers every MMA of this CTA (warpgroup 1 has not waited for it yet)
+        if (ok && n_steps > 0)
+            ok = __all_sync(FULL, mbar_wait(bar_dk, (n_steps - 1) & 1, wd, kSiteDrain));
         if (ok) {
             tc_fence_after();
             const uint32_t tDV = tmem + lane_off + L::kTmDV, tDK = tmem + lane_off + L::kTmDK;
