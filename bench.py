@@ -608,14 +608,33 @@ def oracle_sample(w, budget_s: float):
     f_b = flops_bwd(B, H, n_b, d, w.causal)
     desc = (f"forward on {rows.size} random query rows ({per_head}/head) + backward on the "
             f"{n_b}-token causal prefix, all {B * H} heads; FLOPs counted as on the GPU")
-    return f_f + f_b, t_f + t_b, desc
+    return f_f + f_b, t_f + t_b, desc, rows.size / t_f
 
 
 def run_cpu_baseline(w, budget_s: float):
+    """The oracle on the host cores: all of them, then one thread on a quarter
+    of the budget. Besides TFLOP/s it reports the forward's query rows per
+    second and the time a whole step (forward + backward of the full workload)
+    would take at each rate, labelled as extrapolated."""
     import oracle
-    flops, secs, desc = oracle_sample(w, budget_s)
-    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+    from exact_io_aware_12_gb300.workloads import flops_fwd, flops_bwd
+
+    n_all = oracle.num_threads()
+    flops, secs, desc, rows_s = oracle_sample(w, budget_s)
+    oracle.set_num_threads(1)
+    try:
+        f1, s1, _, rows_s1 = oracle_sample(w, budget_s / 4)
+    finally:
+        oracle.set_num_threads(n_all)
+    B, H, N, d = w.shape
+    full = flops_fwd(B, H, N, d, w.causal) + flops_bwd(B, H, N, d, w.causal)
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": n_all,
+            "kind": "oracle", "sample": desc, "seconds": round(secs, 2),
+            "fwd_rows_per_s": round(rows_s, 1),
+            "single_thread": {"value": round(f1 / s1 / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+                              "fwd_rows_per_s": round(rows_s1, 2), "seconds": round(s1, 2)},
+            "extrapolated_full_step_s": {"all_cores": round(full / (flops / secs), 1),
+                                         "single_thread": round(full / (f1 / s1), 1)}}
 
 
 def run_reference(args):
@@ -630,7 +649,7 @@ def run_reference(args):
         oracle_sample(w, per_step)
     tot_f, tot_s, desc = 0.0, 0.0, ""
     for _ in range(args.steps):
-        f, s, desc = oracle_sample(w, per_step)
+        f, s, desc, _ = oracle_sample(w, per_step)
         tot_f += f
         tot_s += s
     value = tot_f / tot_s / 1e12
