@@ -65,6 +65,9 @@ struct FwdLayout {
     static constexpr uint32_t kTmemS0 = 0, kTmemS1 = TILES == 2 ? 128 : 0;
     static constexpr uint32_t kTmemO0 = TILES == 2 ? 256 : 128, kTmemO1 = TILES == 2 ? 256 + D : 128;
     static constexpr uint32_t kTmemCols = TILES == 2 ? 512 : 256;
+    // d = 64 leaves room for P (bf16, 64 columns per tile) beside S and O, so the
+    // next block's S need not wait for P V (see PIPE in the kernel)
+    static constexpr uint32_t kTmemP0 = TILES == 2 ? 384 : 192, kTmemP1 = TILES == 2 ? 448 : 192;
 };
 
 struct FwdParams {
@@ -85,6 +88,7 @@ struct FwdShared {
     uint64_t kv_full[8];
     uint64_t kv_empty[8];
     uint64_t s_full[2];
+    uint64_t s_free[2];  // PIPE: the softmax has read S_t; its columns may take the next S
     uint64_t p_ready[2];
     uint64_t o_done[2];
     uint32_t tmem_base;
@@ -139,6 +143,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     constexpr int kProducerWarp = 4 * TILES, kMmaWarp = 4 * TILES + 1;
     constexpr bool LOCAL = MASK == kMaskWindow;
     constexpr bool SPARSE = MASK == kMaskBlocks;
+    // d = 64 without a mask: P has its own tensor-memory columns, so S of block
+    // j + 1 is issued as soon as the softmax has read S of block j, and the
+    // softmax runs from block to block without waiting for P V and the next S
+    constexpr bool PIPE = D == 64 && MASK == kMaskNone;
     extern __shared__ uint8_t smem_raw[];
     __shared__ FwdShared sh;
     const uint32_t raw = smem_addr(smem_raw);
@@ -171,6 +179,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const uint32_t bar_kv_full = smem_addr(&sh.kv_full[0]);
     const uint32_t bar_kv_empty = smem_addr(&sh.kv_empty[0]);
     const uint32_t bar_s = smem_addr(&sh.s_full[0]);
+    const uint32_t bar_sf = smem_addr(&sh.s_free[0]);
     const uint32_t bar_p = smem_addr(&sh.p_ready[0]);
     const uint32_t bar_o = smem_addr(&sh.o_done[0]);
 
@@ -183,6 +192,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar_s + 8 * t, 1);
+            mbar_init(bar_sf + 8 * t, 128);
             mbar_init(bar_p + 8 * t, 128);
             mbar_init(bar_o + 8 * t, 1);
         }
@@ -255,9 +265,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     if (ld >= L::kStages &&
                         !mbar_wait(bar_kv_empty + 8 * slot, ((ld / L::kStages) - 1) & 1, wd, kSiteProdEmpty))
                         break;
-                    const CUtensorMap* map = (ld & 1) ? &tmV : &tmK;
-                    const uint32_t dst = sbase + L::kRing + slot * L::kTileBytes;
+                    bool is_k = (ld & 1) == 0;
                     int blk = jlo + (ld >> 1);
+                    if constexpr (PIPE) {
+                        // the MMA warp's order: K0 K1 V0 K2 V1 ... K(nb-1) V(nb-2) V(nb-1)
+                        is_k = ld == 0 || ((ld & 1) && ld < 2 * nb - 1);
+                        blk = is_k ? (ld + 1) / 2 : (ld == 2 * nb - 1 ? nb - 1 : ld / 2 - 1);
+                    }
+                    const CUtensorMap* map = is_k ? &tmK : &tmV;
+                    const uint32_t dst = sbase + L::kRing + slot * L::kTileBytes;
                     if constexpr (SPARSE) {
                         if ((ld & 1) == 0) jb = next_set_bit(sh.use[0], sh.use[1], jb + 1, n_kv);
                         blk = jb;
@@ -340,6 +356,58 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                             mma_commit_warp(bar_kv_empty + 8 * sv);
                             if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
                             j = jn;
+                        }
+                    }
+                } else if constexpr (PIPE) {
+                    // iteration j issues S(j) of both tiles (each once the softmax has
+                    // read S(j - 1)), then P(j - 1) V(j - 1) of both tiles
+                    const int hi[2] = {hi0, n_blk1 > 0 ? hi1 : 0};
+                    const uint32_t tP[2] = {tmem + L::kTmemP0, tmem + L::kTmemP1};
+                    bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteMmaQ));
+                    for (int j = 0; ok && j <= nb; ++j) {
+                        if (j < nb) {
+                            const int lk = j == 0 ? 0 : 2 * j - 1, sk = lk % L::kStages;  // K_j
+                            if (!__all_sync(0xffffffffu, mbar_wait(bar_kv_full + 8 * sk,
+                                                                   (lk / L::kStages) & 1, wd, kSiteMmaKV))) {
+                                ok = false;
+                                break;
+                            }
+#pragma unroll
+                            for (int t = 0; t < TILES; ++t) {
+                                if (ok && j < hi[t]) {
+                                    if (j > 0)
+                                        ok = __all_sync(0xffffffffu, mbar_wait(bar_sf + 8 * t, (j - 1) & 1, wd,
+                                                                               kSiteMmaP));
+                                    if (ok) {
+                                        tc_fence_after();
+                                        issue_s<D>(tS[t], qlo[t], klo0 + sk * kSlot);
+                                        mma_commit_warp(bar_s + 8 * t);
+                                    }
+                                }
+                            }
+                            if (!ok) break;
+                            mma_commit_warp(bar_kv_empty + 8 * sk);
+                        }
+                        if (j > 0) {
+                            const int lv = min(2 * j, 2 * nb - 1), sv = lv % L::kStages;  // V_(j-1)
+                            if (!__all_sync(0xffffffffu, mbar_wait(bar_kv_full + 8 * sv,
+                                                                   (lv / L::kStages) & 1, wd, kSiteMmaKV))) {
+                                ok = false;
+                                break;
+                            }
+#pragma unroll
+                            for (int t = 0; t < TILES; ++t) {
+                                if (ok && j - 1 < hi[t]) {
+                                    ok = __all_sync(0xffffffffu, mbar_wait(bar_p + 8 * t, (j - 1) & 1, wd, kSiteMmaP));
+                                    if (ok) {
+                                        tc_fence_after();
+                                        issue_pv<D>(tO[t], tP[t], vlo0 + sv * kSlot, j > 1);
+                                        mma_commit_warp(bar_o + 8 * t);
+                                    }
+                                }
+                            }
+                            if (!ok) break;
+                            mma_commit_warp(bar_kv_empty + 8 * sv);
                         }
                     }
                 } else {
@@ -457,7 +525,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_off + (t ? L::kTmemS1 : L::kTmemS0);
         const uint32_t tO = tmem + lane_off + (t ? L::kTmemO1 : L::kTmemO0);
+        // P: over S, or (PIPE) in its own columns
+        const uint32_t tP = PIPE ? tmem + lane_off + (t ? L::kTmemP1 : L::kTmemP0) : tS;
         const uint32_t my_s = bar_s + 8 * t, my_p = bar_p + 8 * t, my_o = bar_o + 8 * t;
+        const uint32_t my_sf = bar_sf + 8 * t;
         const float sl2 = p.scale_log2;
         float m_used = -INFINITY;
         float l = 0.f, l_mma = 0.f;
@@ -484,6 +555,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tmem_ld_wait(s[1]);
             tmem_ld_wait(s[2]);
             tmem_ld_wait(s[3]);
+            if constexpr (PIPE) {
+                tc_fence_before();
+                mbar_arrive(my_sf);  // S's columns may take the next block's scores now
+            }
 
             const int kbase = j * kBN;
             const bool need_mask = (CAUSAL && kbase + kBN - 1 > q_start) || (kbase + kBN > N) ||
@@ -540,8 +615,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     lr0 += u2f(pk[i] << 16);
                     lr1 += u2f(pk[i] & 0xffff0000u);
                 }
-                tmem_st32(tS + h * 32, pk);
+                if (PIPE && h == 0 && jj > 0) {
+                    // P's columns are free once the previous P V has read them
+                    if (!__all_sync(0xffffffffu, mbar_wait(my_o, (jj - 1) & 1, wd, kSiteSoftO))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                tmem_st32(tP + h * 32, pk);
             }
+            if (!ok) break;
             l += ls0 + ls1;
             l_mma += lr0 + lr1;
             if (jj > 0 && __any_sync(0xffffffffu, grow)) {
