@@ -147,6 +147,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // j + 1 is issued as soon as the softmax has read S of block j, and the
     // softmax runs from block to block without waiting for P V and the next S
     constexpr bool PIPE = D == 64 && MASK == kMaskNone;
+    // the row sums as paired fp32 adds (bitwise the same sums): measured faster
+    // in the one-tile kernel, slower in the two-tile one (register pressure)
+    constexpr bool PAIRED_SUMS = PIPE && TILES == 1;
     extern __shared__ uint8_t smem_raw[];
     __shared__ FwdShared sh;
     const uint32_t raw = smem_addr(smem_raw);
@@ -600,6 +603,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // the scale-and-subtract runs as one paired fp32 FMA per two scores
             const uint64_t c2 = f2_pack(sl2, sl2), nm2 = f2_pack(neg_m, neg_m);
             float ls0 = 0.f, ls1 = 0.f, lr0 = 0.f, lr1 = 0.f;
+            uint64_t ls2 = 0, lr2 = 0;  // PAIRED_SUMS: the same sums, paired
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t pk[32];
@@ -610,10 +614,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         f2_pack(u2f(s[c >> 5][c & 31]), u2f(s[c >> 5][(c & 31) + 1])), c2, nm2));
                     const float p0 = ex2(x.x), p1 = ex2(x.y);
                     pk[i] = pack_bf16(p0, p1);
-                    ls0 += p0;
-                    ls1 += p1;
-                    lr0 += u2f(pk[i] << 16);
-                    lr1 += u2f(pk[i] & 0xffff0000u);
+                    if constexpr (PAIRED_SUMS) {
+                        ls2 = fadd2(ls2, f2_pack(p0, p1));
+                        lr2 = fadd2(lr2, f2_pack(u2f(pk[i] << 16), u2f(pk[i] & 0xffff0000u)));
+                    } else {
+                        ls0 += p0;
+                        ls1 += p1;
+                        lr0 += u2f(pk[i] << 16);
+                        lr1 += u2f(pk[i] & 0xffff0000u);
+                    }
                 }
                 if (PIPE && h == 0 && jj > 0) {
                     // P's columns are free once the previous P V has read them
@@ -626,6 +635,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 tmem_st32(tP + h * 32, pk);
             }
             if (!ok) break;
+            if constexpr (PAIRED_SUMS) {
+                const float2 a2 = f2_unpack(ls2), b2 = f2_unpack(lr2);
+                ls0 = a2.x;
+                ls1 = a2.y;
+                lr0 = b2.x;
+                lr1 = b2.y;
+            }
             l += ls0 + ls1;
             l_mma += lr0 + lr1;
             if (jj > 0 && __any_sync(0xffffffffu, grow)) {
