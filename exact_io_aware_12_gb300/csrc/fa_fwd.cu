@@ -149,7 +149,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     constexpr bool PIPE = D == 64 && MASK == kMaskNone;
     // the row sums as paired fp32 adds (bitwise the same sums): measured faster
     // in the one-tile kernel, slower in the two-tile one (register pressure)
-    constexpr bool PAIRED_SUMS = PIPE && TILES == 1;
+    constexpr bool PAIRED_SUMS = (PIPE && TILES == 1) || (D == 128 && MASK == kMaskNone && !O32);
+    // P is converted and stored in chunks of kPC packed columns: 16 at d = 128, which
+    // frees the registers the paired sums need there, 32 at d = 64 and for the fp32
+    // O (measured faster, and without spills, there)
+    constexpr int kPC = (D == 128 && !O32) ? 16 : 32;
     extern __shared__ uint8_t smem_raw[];
     __shared__ FwdShared sh;
     const uint32_t raw = smem_addr(smem_raw);
@@ -603,13 +607,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // the scale-and-subtract runs as one paired fp32 FMA per two scores
             const uint64_t c2 = f2_pack(sl2, sl2), nm2 = f2_pack(neg_m, neg_m);
             float ls0 = 0.f, ls1 = 0.f, lr0 = 0.f, lr1 = 0.f;
-            uint64_t ls2 = 0, lr2 = 0;  // PAIRED_SUMS: the same sums, paired
+            uint64_t ls2 = 0, lr2 = 0;  // PAIRED_SUMS: the same sums, paired (bitwise equal)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
+            for (int h = 0; h < 64 / kPC; ++h) {
+                uint32_t pk[kPC];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = h * 64 + 2 * i;
+                for (int i = 0; i < kPC; ++i) {
+                    const int c = h * 2 * kPC + 2 * i;
                     const float2 x = f2_unpack(ffma2(
                         f2_pack(u2f(s[c >> 5][c & 31]), u2f(s[c >> 5][(c & 31) + 1])), c2, nm2));
                     const float p0 = ex2(x.x), p1 = ex2(x.y);
@@ -632,7 +636,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                     }
                     tc_fence_after();
                 }
-                tmem_st32(tP + h * 32, pk);
+                if constexpr (kPC == 16) tmem_st16(tP + h * 16, pk);
+                else tmem_st32(tP + h * 32, pk);
             }
             if (!ok) break;
             if constexpr (PAIRED_SUMS) {
