@@ -21,7 +21,11 @@
 //     other tile's MMAs;
 //   - the exponent is taken with ex2 on tau*log2(e)-scaled scores; O is
 //     rescaled only when a row's max grows by more than 2^8 (the stale max
-//     is used for both O and l, so the final O / l is unchanged);
+//     is used for both O and l, so the final O / l is unchanged); the row
+//     sums run as paired fp32 adds where the registers allow it;
+//   - at d = 128 P is written over S, so a tile's next S waits for its P V;
+//     at d = 64 (no mask) P has columns of its own and the next S is issued
+//     as soon as the softmax has read S (PIPE below);
 //   - causal: key blocks wholly above the diagonal are never loaded; the
 //     diagonal block is masked element-wise.  Keys >= N in a ragged last
 //     block are masked the same way.
