@@ -414,6 +414,66 @@ def measure_variant(w, q, k, v, do, dev, steps, peak, ff, **mask):
             "flops_fwd": ff}
 
 
+SWEEP_TOKENS = 16 * 16384  # B*H*N of every sweep shape (the 16k workload's)
+
+
+def run_sweep(args):
+    """Shape sweep (--sweep): d in {64, 128}, causal and not, N = 1024 ... 32768
+    at a fixed token count B*H*N (H = 16, B = tokens / (16 N), or H = 8 at
+    N = 32768); per shape the forward and backward main kernels' CUDA-event
+    times over --steps calls (L2 flushed before each), one JSON line each.
+    Seeded N(0, 1) inputs; TFLOP/s on the causal-halved FLOP count."""
+    import torch
+    from exact_io_aware_12_gb300 import api, _lib
+    from exact_io_aware_12_gb300.workloads import draw, flops_fwd
+
+    dev = torch.device("cuda", 0)
+    peaks, src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for d in (64, 128):
+        for causal in (True, False):
+            for N in (1024, 2048, 4096, 8192, 16384, 32768):
+                H = 16 if N < 32768 else 8
+                B = max(1, SWEEP_TOKENS // (H * N))
+                x = draw(B, H, N, d, seed=N + d)
+                q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+                tau = 1 / math.sqrt(d)
+                o = torch.empty_like(q)
+                lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+                dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+                ws = torch.empty(api.workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+                for _ in range(args.warmup):
+                    api.fwd(q, k, v, causal, tau, out=o, lse=lse)
+                    api.bwd(q, k, v, o, do, lse, causal, tau, dq=dq, dk=dk, dv=dv, workspace=ws)
+                ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+                for e in sum(ev, []):
+                    e.record(stream)
+                torch.cuda.synchronize(dev)
+                for i in range(args.steps):
+                    flush.fill_(float(i))
+                    _lib.check(_lib.fa_set_timing_events(ev[i][0].cuda_event, ev[i][1].cuda_event), "timing")
+                    api.fwd(q, k, v, causal, tau, out=o, lse=lse)
+                    _lib.check(_lib.fa_set_timing_events(ev[i][2].cuda_event, ev[i][3].cuda_event), "timing")
+                    api.bwd(q, k, v, o, do, lse, causal, tau, dq=dq, dk=dk, dv=dv, workspace=ws)
+                    _lib.check(_lib.fa_set_timing_events(None, None), "timing")
+                torch.cuda.synchronize(dev)
+                if api.last_device_error(dev) != _lib.FA_OK:
+                    raise RuntimeError("kernel watchdog fired in the sweep")
+                fms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+                bms = sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps
+                ff = flops_fwd(B, H, N, d, causal)
+                print(json.dumps({"sweep": True, "B": B, "H": H, "N": N, "d": d, "causal": causal,
+                                  "fwd_ms": round(fms, 4), "fwd_tflops": round(ff / fms / 1e9, 1),
+                                  "fwd_frac": round(ff / fms / 1e9 / peak, 4),
+                                  "bwd_main_ms": round(bms, 4),
+                                  "bwd_tflops": round(2.5 * ff / bms / 1e9, 1),
+                                  "bwd_frac": round(2.5 * ff / bms / 1e9 / peak, 4),
+                                  "peak_tflops": peak, "peak_source": src}), flush=True)
+                del q, k, v, do, o, lse, dq, dk, dv, ws, x
+
+
 def measure_window(w, q, k, v, do, dev, window, steps, peak):
     """Causal sliding window of `window` keys (fa_fwd_window / fa_bwd_window)."""
     B, H, N, d = w.shape
@@ -686,6 +746,8 @@ def main(argv=None):
     ap.add_argument("--no-decode", dest="decode", action="store_false",
                     help="skip the decode leg")
     ap.add_argument("--no-fp8", dest="fp8", action="store_false", help="skip the FP8 leg")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the bench line: forward/backward TFLOP/s over d, causal and N")
     ap.add_argument("--decode-shape", default="8,16,1,32768,128",
                     help="B,H,Nq,Nk,d of the decode leg (a smaller case: profiling only)")
     args = ap.parse_args(argv)
@@ -696,6 +758,8 @@ def main(argv=None):
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world} (launch N>1 with torchrun)")
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_ours(args)
 
