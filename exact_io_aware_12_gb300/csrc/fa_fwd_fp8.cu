@@ -17,10 +17,9 @@
 //     as e4m3, not bf16: each softmax thread converts its row of P
 //     (cvt.rn.satfinite.e4m3x2), packs four keys per 32-bit column and writes
 //     the 32 columns over its tile's S, where the P V product reads it as the
-//     A operand (A from tensor memory, V from shared memory).  With P in shared
-//     memory instead, every MMA of the loop reads both operands from shared
-//     memory, which then carries about 1.5 times the MMAs' own cycles per
-//     block and slows them down;
+//     A operand (A from tensor memory, V from shared memory).  A version with
+//     P staged in shared memory ran at the same speed; this one moves 64 KB
+//     less through shared memory per key block and needs no proxy fences;
 //   - P = 2^(x - m + 6) with the row max m rescaled only when it grows by more
 //     than 2^2: P stays <= 2^8 (e4m3 saturates at 448) and the smallest
 //     weights sit 2^6 further above e4m3's subnormal range than with P <= 1;
