@@ -42,10 +42,9 @@ namespace {
 
 constexpr int kBQ = 128;  // query rows per step
 constexpr int kBK = 128;  // keys per CTA
-constexpr int kThreads = 352;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kReducerWarp = 10;
+// NWG elementwise warpgroups (warps 0 .. 4 NWG - 1), then the loader, MMA and
+// reducer warps.
+constexpr int bwd_threads(int nwg) { return 32 * (4 * nwg + 3); }
 constexpr float kLog2e = 1.44269504088896341f;
 // Which query tiles a key tile visits beyond causality.
 enum : int { kMaskNone = 0, kMaskWindow = 1, kMaskBlocks = 2 };
@@ -83,8 +82,8 @@ struct BwdBarriers {
     uint64_t ds_ready;
     uint64_t dq_full;
     uint64_t dq_drained;
-    uint64_t dq_staged_q;   // warpgroup 0 staged its dQ half (over Q)
-    uint64_t dq_staged_do;  // warpgroup 1 staged its dQ half (over dO)
+    uint64_t dq_staged_q;   // the warpgroups of dQ columns [0, D/2) staged them (over Q)
+    uint64_t dq_staged_do;  // the warpgroups of dQ columns [D/2, D) staged them (over dO)
     uint64_t dk_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -130,10 +129,10 @@ __device__ __forceinline__ void mma_rows_rows(uint32_t tmem_d, uint32_t a_lo, ui
 }
 
 // D (+)= A_tmem[128 x 128] B, B an MN-major smem tile [128 rows(K) x N] (N = Dn).
-// A (bf16, packed two per column) holds K-columns 0-63 at tensor-memory columns
-// [0, 32) and K-columns 64-127 at [64, 96): each half is written by its own
-// warpgroup over the fp32 values it has already read.
-template <int Dn>
+// A (bf16, packed two per column): each warpgroup owns QC consecutive K-columns
+// (queries) and writes them packed over the first QC/2 of its QC fp32 columns,
+// so K-columns [g QC, (g + 1) QC) sit at tensor-memory columns [g QC, g QC + QC/2).
+template <int Dn, int QC>
 __device__ __forceinline__ void mma_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint32_t b_lo,
                                            bool accumulate) {
     constexpr uint32_t id = idesc_bf16(128, Dn, false, true);
@@ -141,8 +140,8 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uin
     else mma_ts_warp<0>(tmem_d, tmem_a, b_lo, kDescHi, id);
 #pragma unroll
     for (int k = 1; k < 128 / 16; ++k)
-        mma_ts_warp<1>(tmem_d, tmem_a + (k >> 2) * 64 + (k & 3) * 8, b_lo + ((k * 2048) >> 4),
-                     kDescHi, id);
+        mma_ts_warp<1>(tmem_d, tmem_a + (16 * k / QC) * QC + (16 * k % QC) / 2,
+                       b_lo + ((k * 2048) >> 4), kDescHi, id);
 }
 
 // D = A B with A MN-major [128(K) x 128(M)] and B MN-major [128(K) x Dn].
@@ -157,8 +156,8 @@ __device__ __forceinline__ void mma_mn_mn(uint32_t tmem_d, uint32_t a_lo, uint32
 
 // MASK: kMaskNone; kMaskWindow, a causal sliding window of p.window keys (only
 // with CAUSAL); kMaskBlocks, the block mask p.blocks.
-template <int D, bool CAUSAL, int MASK>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool CAUSAL, int MASK, int NWG>
+__global__ void __launch_bounds__(bwd_threads(NWG), 1)
 fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                    const __grid_constant__ CUtensorMap tmdQacc,
@@ -166,6 +165,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                    const BwdParams p) {
     using L = BwdLayout<D>;
     static_assert(sizeof(BwdBarriers) <= L::kBytes - L::kBars, "barrier block overflows its slot");
+    static_assert(NWG == 2 || (NWG == 4 && D == 128), "four warpgroups need 32-column drain boxes");
+    constexpr int kProducerWarp = 4 * NWG, kMmaWarp = 4 * NWG + 1, kReducerWarp = 4 * NWG + 2;
+    constexpr int kQC = 128 / NWG;      // query columns of P^T / dS^T per warpgroup
+    constexpr int kDC = D / NWG;        // d-columns of dQ, dK, dV per warpgroup
+    constexpr int kEW = 128 * NWG;      // elementwise threads
     constexpr bool LOCAL = MASK == kMaskWindow;
     constexpr bool SPARSE = MASK == kMaskBlocks;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -219,12 +223,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
         mbar_init(bar_s, 1);
         mbar_init(bar_dp, 1);
-        mbar_init(bar_p, 256);
-        mbar_init(bar_ds, 256);
+        mbar_init(bar_p, kEW);
+        mbar_init(bar_ds, kEW);
         mbar_init(bar_dq, 1);
-        mbar_init(bar_dr, 256);
-        mbar_init(bar_sgq, 128);
-        mbar_init(bar_sgd, 128);
+        mbar_init(bar_dr, kEW);
+        mbar_init(bar_sgq, kEW / 2);
+        mbar_init(bar_sgd, kEW / 2);
         mbar_init(bar_dk, 1);
         mbar_init_fence();
     }
@@ -354,7 +358,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 const uint32_t so = st * kStageStep;
                 if (!__all_sync(0xffffffffu, mbar_wait(bar_p, s & 1, wd, kSiteMmaP))) { ok = false; break; }
                 tc_fence_after();
-                mma_tmem_a<D>(tmem + L::kTmDV, tmem + L::kTmS, do_mn0 + so, s > 0);   // dV
+                mma_tmem_a<D, kQC>(tmem + L::kTmDV, tmem + L::kTmS, do_mn0 + so, s > 0);   // dV
                 mma_commit_warp(bar_de + 8 * st);  // the last MMA that reads this dO
                 if (!__all_sync(0xffffffffu, mbar_wait(bar_ds, s & 1, wd, kSiteMmaDS))) { ok = false; break; }
                 tc_fence_after();
@@ -366,7 +370,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 }
                 mma_mn_mn<D>(tmem + L::kTmDQ, ds_mn, k_mn);                            // dQ
                 mma_commit_warp(bar_dq);
-                mma_tmem_a<D>(tmem + L::kTmDK, tmem + L::kTmDP, q_mn0 + so, s > 0);   // dK
+                mma_tmem_a<D, kQC>(tmem + L::kTmDK, tmem + L::kTmDP, q_mn0 + so, s > 0);   // dK
                 mma_commit_warp(bar_dk);
                 mma_commit_warp(bar_qe + 8 * st);
                 if (s + 1 < n_steps) {
@@ -413,8 +417,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 }
                 const uint32_t src = sbase + L::kStage0 + st * L::kStageBytes;
                 const int q_start = qtile * kBQ;
-                // dQ columns [D/2, D) were staged over dO (warpgroup 1, first),
-                // [0, D/2) over Q (warpgroup 0, once dK is done)
+                // dQ columns [D/2, D) were staged over dO (first), [0, D/2) over Q
+                // (once dK is done)
                 if (ok) ok = mbar_wait(bar_sgd, s & 1, wd, kSiteReduce);
                 if (ok) {
                     for (int b = D / 64; b < D / 32; ++b)
@@ -435,21 +439,24 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
         __syncwarp();
     } else {
-        // ------------------------- warpgroups 0 and 1 (warps 0-3 and 4-7) --
-        // Warpgroup h owns query columns [64h, 64h + 64) of P^T and dS^T, and
-        // d-columns [h D/2, (h + 1) D/2) of the dQ drain and the dK/dV epilogue.
+        // ------------------------------------- elementwise warpgroups 0 .. NWG-1 --
+        // Warpgroup h owns query columns [kQC h, kQC (h + 1)) of P^T and dS^T, and
+        // d-columns [kDC h, kDC (h + 1)) of the dQ drain and the dK/dV epilogue.
         // A failed wait poisons the rest of the work (ok = false) but every
         // thread still reaches every named barrier, so none can be left waiting.
         const int h = warp >> 2;
         const int r = threadIdx.x & 127;  // key row (P^T, dS^T, dK, dV) / query row (dQ)
         const int kg = kv_start + r;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_off + L::kTmS + 64 * h;
-        const uint32_t tDP = tmem + lane_off + L::kTmDP + 64 * h;
-        const uint32_t tDQ = tmem + lane_off + L::kTmDQ + h * (D / 2);
+        const uint32_t tS = tmem + lane_off + L::kTmS + kQC * h;
+        const uint32_t tDP = tmem + lane_off + L::kTmDP + kQC * h;
+        const uint32_t tDQ = tmem + lane_off + L::kTmDQ + kDC * h;
         const float sl2 = p.scale_log2;
-        uint8_t* ds_row = smem + L::kDS + h * (128 * 128) + r * 128;
-        constexpr int kDrainBoxes = D / 64;  // fp32 boxes of 32 columns per warpgroup
+        // this row of the dS^T tile: the box (64 query columns) holding this warpgroup's
+        // columns, and their first 16-byte chunk in it
+        uint8_t* ds_row = smem + L::kDS + (kQC * h / 64) * (128 * 128) + r * 128;
+        const int ds_chunk0 = (kQC * h % 64) / 8;
+        constexpr int kDrainBoxes = kDC / 32;  // fp32 boxes of 32 columns per warpgroup
         bool ok = true;
         int qsp = -1;  // block mask: the query tile of the last step
         for (int s = 0; s < n_steps; ++s) {
@@ -467,14 +474,14 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 tc_fence_after();
                 // -log2(e) LSE per query, pairs of adjacent queries as one 64-bit value,
                 // read four queries per 16-byte broadcast load
-                const ulonglong2* nl4 = reinterpret_cast<const ulonglong2*>(lse2_s + st * 128 + 64 * h);
+                const ulonglong2* nl4 = reinterpret_cast<const ulonglong2*>(lse2_s + st * 128 + kQC * h);
                 const bool diag = CAUSAL && (q_start == kv_start);
                 // window edge: query q no longer sees key kg once q >= kg + window
                 const bool wedge = window > 0 && q_start + kBQ - 1 >= kv_start + window;
-                const int qh = q_start + 64 * h;
+                const int qh = q_start + kQC * h;
                 const uint64_t c2 = f2_pack(sl2, sl2);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < kQC / 32; ++c) {
                     uint32_t sv[32];
                     tmem_ld32(tS + 32 * c, sv);
                     tmem_ld_wait(sv);
@@ -516,9 +523,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             if (ok) {
                 tc_fence_after();
                 // -D per query, pairs of adjacent queries as one 64-bit value (16-byte loads)
-                const ulonglong2* nd4 = reinterpret_cast<const ulonglong2*>(dvec_s + st * 128 + 64 * h);
+                const ulonglong2* nd4 = reinterpret_cast<const ulonglong2*>(dvec_s + st * 128 + kQC * h);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < kQC / 32; ++c) {
                     uint32_t dp[32], pk[16];
                     tmem_ld32(tDP + 32 * c, dp);
                     tmem_ld16(tS + 16 * c, pk);
@@ -539,7 +546,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     tmem_st16(tDP + 16 * c, ds);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
-                        const int chunk = 4 * c + q4;
+                        const int chunk = ds_chunk0 + 4 * c + q4;
                         *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
                             make_uint4(ds[4 * q4], ds[4 * q4 + 1], ds[4 * q4 + 2], ds[4 * q4 + 3]);
                     }
@@ -564,7 +571,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 mbar_arrive(bar_dr);
                 // stage fp32 boxes of [128 x 32] over this step's Q (warpgroup 0) and dO
                 // (warpgroup 1): dO is free (dV, dP^T done before dQ), Q once dK is
-                if (h == 0) ok = __all_sync(FULL, mbar_wait(bar_dk, s & 1, wd, kSiteDrain));
+                if (h < NWG / 2) ok = __all_sync(FULL, mbar_wait(bar_dk, s & 1, wd, kSiteDrain));
             } else {
                 mbar_arrive(bar_dr);
             }
@@ -580,7 +587,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 }
                 fence_async_shared();
             }
-            mbar_arrive(h ? bar_sgd : bar_sgq);  // the reducer warp adds the staged tiles into dQ
+            mbar_arrive(h >= NWG / 2 ? bar_sgd : bar_sgq);  // the reducer adds the staged tiles into dQ
         }
         // dK = tau * dK_acc and dV (this warpgroup's D/2 columns), staged over the K
         // and V tiles, which no MMA reads any more: the commit after the last dK
@@ -596,8 +603,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 const float scale = which ? p.tau : 1.f;
                 const uint32_t src = which ? tDK : tDV;
 #pragma unroll
-                for (int cc = 0; cc < D / 2; cc += 32) {
-                    const int c0 = h * (D / 2) + cc;
+                for (int cc = 0; cc < kDC; cc += 32) {
+                    const int c0 = h * kDC + cc;
                     uint32_t o[32];
                     if (!SPARSE || n_steps > 0) {
                         tmem_ld32(src + c0, o);
@@ -622,7 +629,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             }
             fence_async_shared();
         }
-        named_bar_sync(4, 256);
+        named_bar_sync(4, kEW);
         if (threadIdx.x == 0 && ok) {
             for (int b = 0; b < L::kBoxes; ++b) {
                 tma_store_3d(&tmdV, sbase + L::kV + b * L::kBox, b * 64, kv_start, bh);
@@ -717,7 +724,9 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
             !make_tile_map(&tdk, a.dK, BF, 2, D, a.N, a.BH, 64, kBK) ||
             !make_tile_map(&tdv, a.dV, BF, 2, D, a.N, a.BH, 64, kBK))
             return cudaErrorInvalidValue;
-        auto kern = fa_bwd_main_kernel<D, CAUSAL, MASK>;
+        // d = 128: four elementwise warpgroups (each half the columns of two)
+        constexpr int NWG = D == 128 ? 4 : 2;
+        auto kern = fa_bwd_main_kernel<D, CAUSAL, MASK, NWG>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
         if (e != cudaSuccess) return e;
         BwdParams p;
@@ -734,7 +743,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         p.wait_limit_ns = a.wait_limit_ns;
         dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(p.n_kv));
         if (a.ev_start) cudaEventRecord(a.ev_start, stream);
-        kern<<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tacc, tdk, tdv, p);
+        kern<<<grid, bwd_threads(NWG), L::kBytes, stream>>>(tq, tk, tv, tdo, tacc, tdk, tdv, p);
         e = cudaGetLastError();
         if (e == cudaSuccess && a.ev_stop) e = cudaEventRecord(a.ev_stop, stream);
         if (e != cudaSuccess) return e;
