@@ -14,18 +14,19 @@
 //             diagonal when causal):
 //               S^T  = K Q_i^T            tcgen05, both operands in smem
 //               dP^T = V dO_i^T           tcgen05
-//               P^T  = exp2(c S^T - log2e LSE_i)   warps 0-7, written back to
-//                                         tensor memory as bf16 over S^T
+//               P^T  = exp2(c S^T - log2e LSE_i)   elementwise warps, written
+//                                         back to tensor memory as bf16 over S^T
 //               dV  += P^T dO_i           tcgen05, A read from tensor memory
-//               dS^T = P^T o (dP^T - D_i) warps 0-7, to tensor memory (over
-//                                         dP^T) and to smem
+//               dS^T = P^T o (dP^T - D_i) elementwise warps, to tensor memory
+//                                         (over dP^T) and to smem
 //               dK  += dS^T Q_i           tcgen05, A from tensor memory
 //               dQ_i = dS K               tcgen05, A = dS^T from smem
-//             warps 0-7 (two warpgroups, each half of the query columns)
-//             also read dQ_i out of tensor memory into fp32 smem tiles that
-//             warp 10 adds into the accumulator with TMA bulk reductions (no
-//             per-element atomics); at the end they write dK (scaled by tau)
-//             and dV.  Warp 8 loads (TMA), warp 9 issues the MMAs.
+//             the elementwise warps (NWG warpgroups: four at d = 128, two at
+//             d = 64, each a share of the query columns) also read dQ_i out of
+//             tensor memory into fp32 smem tiles that the reducer warp adds
+//             into the accumulator with TMA bulk reductions (no per-element
+//             atomics); at the end they write dK (scaled by tau) and dV.  The
+//             loader warp issues the TMA copies, the MMA warp the MMAs.
 //   bwd_post  dQ = bf16(tau * accumulator).
 // Tensor memory (512 columns): dV and dK accumulators (d each), S^T (128),
 // dP^T (128); for d = 128 the dQ tile reuses the S^T columns once P^T has
