@@ -468,14 +468,20 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 qtile = qsp;
             }
             const int q_start = qtile * kBQ;
-            // P^T = exp2(c S^T - log2e LSE), bf16, over this warpgroup's S^T columns
-            if (ok) ok = __all_sync(FULL, mbar_wait(bar_s, s & 1, wd, kSiteDsS) &&
-                                              mbar_wait(bar_qf + 8 * st, (s >> 1) & 1, wd, kSiteDsQ));
+            // P^T = exp2(c S^T - log2e LSE), bf16, over this warpgroup's S^T columns.
+            // -log2(e) LSE per query, pairs of adjacent queries as one 64-bit value,
+            // read four queries per 16-byte broadcast load; the first chunk's are
+            // read as soon as the stage (with the vectors) is in, before S^T is
+            const ulonglong2* nl4 = reinterpret_cast<const ulonglong2*>(lse2_s + st * 128 + kQC * h);
+            ulonglong2 nl0[8];
+            if (ok) ok = __all_sync(FULL, mbar_wait(bar_qf + 8 * st, (s >> 1) & 1, wd, kSiteDsQ));
+            if (ok) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) nl0[i] = nl4[i];
+            }
+            if (ok) ok = __all_sync(FULL, mbar_wait(bar_s, s & 1, wd, kSiteDsS));
             if (ok) {
                 tc_fence_after();
-                // -log2(e) LSE per query, pairs of adjacent queries as one 64-bit value,
-                // read four queries per 16-byte broadcast load
-                const ulonglong2* nl4 = reinterpret_cast<const ulonglong2*>(lse2_s + st * 128 + kQC * h);
                 const bool diag = CAUSAL && (q_start == kv_start);
                 // window edge: query q no longer sees key kg once q >= kg + window
                 const bool wedge = window > 0 && q_start + kBQ - 1 >= kv_start + window;
@@ -489,7 +495,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     uint32_t pk[16];
                     ulonglong2 nl[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) nl[i] = nl4[8 * c + i];
+                    for (int i = 0; i < 8; ++i) nl[i] = c == 0 ? nl0[i] : nl4[8 * c + i];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int q = 32 * c + 2 * i;
@@ -518,13 +524,19 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             }
             mbar_arrive(bar_p);
 
-            // dS^T = P^T o (dP^T - D), to tensor memory (over dP^T) and to smem
+            // dS^T = P^T o (dP^T - D), to tensor memory (over dP^T) and to smem.
+            // -D per query, pairs of adjacent queries as one 64-bit value (16-byte
+            // loads); the first chunk's are read before the wait for dP^T
+            const ulonglong2* nd4 = reinterpret_cast<const ulonglong2*>(dvec_s + st * 128 + kQC * h);
+            ulonglong2 nd0[8];
+            if (ok) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) nd0[i] = nd4[i];
+            }
             if (ok) ok = __all_sync(FULL, mbar_wait(bar_dp, s & 1, wd, kSiteDsDP) &&
                                               (s == 0 || mbar_wait(bar_dq, (s - 1) & 1, wd, kSiteDsDQ)));
             if (ok) {
                 tc_fence_after();
-                // -D per query, pairs of adjacent queries as one 64-bit value (16-byte loads)
-                const ulonglong2* nd4 = reinterpret_cast<const ulonglong2*>(dvec_s + st * 128 + kQC * h);
 #pragma unroll
                 for (int c = 0; c < kQC / 32; ++c) {
                     uint32_t dp[32], pk[16];
@@ -535,7 +547,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     uint32_t ds[16];
                     ulonglong2 nd[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) nd[i] = nd4[8 * c + i];
+                    for (int i = 0; i < 8; ++i) nd[i] = c == 0 ? nd0[i] : nd4[8 * c + i];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const uint64_t ndq = (i & 1) ? nd[i >> 1].y : nd[i >> 1].x;
