@@ -474,6 +474,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             // read as soon as the stage (with the vectors) is in, before S^T is
             const ulonglong2* nl4 = reinterpret_cast<const ulonglong2*>(lse2_s + st * 128 + kQC * h);
             ulonglong2 nl0[8];
+            uint32_t pkeep[16];  // the first chunk's packed P^T, reused by dS^T below
             if (ok) ok = __all_sync(FULL, mbar_wait(bar_qf + 8 * st, (s >> 1) & 1, wd, kSiteDsQ));
             if (ok) {
 #pragma unroll
@@ -518,6 +519,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                         pk[i] = pack_bf16(p0, p1);
                     }
                     tmem_st16(tS + 16 * c, pk);
+                    if (c == 0) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) pkeep[i] = pk[i];
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -541,9 +546,14 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int c = 0; c < kQC / 32; ++c) {
                     uint32_t dp[32], pk[16];
                     tmem_ld32(tDP + 32 * c, dp);
-                    tmem_ld16(tS + 16 * c, pk);
+                    if (c == 0) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) pk[i] = pkeep[i];
+                    } else {
+                        tmem_ld16(tS + 16 * c, pk);
+                        tmem_ld_wait(pk);
+                    }
                     tmem_ld_wait(dp);
-                    tmem_ld_wait(pk);
                     uint32_t ds[16];
                     ulonglong2 nd[8];
 #pragma unroll
