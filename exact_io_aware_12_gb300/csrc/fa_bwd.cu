@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <type_traits>
 
 #include "fa_internal.h"
 #include "ptx.cuh"
@@ -488,6 +489,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 const bool wedge = window > 0 && q_start + kBQ - 1 >= kv_start + window;
                 const int qh = q_start + kQC * h;
                 const uint64_t c2 = f2_pack(sl2, sl2);
+                // most tiles need no mask: the loop is built twice, and the masked
+                // copy runs only on the diagonal, window-edge and ragged-end tiles
+                const bool masked = diag || wedge || kv_start + kBK > N;
 #pragma unroll
                 for (int c = 0; c < kQC / 32; ++c) {
                     uint32_t sv[32];
@@ -497,27 +501,33 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     ulonglong2 nl[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) nl[i] = c == 0 ? nl0[i] : nl4[8 * c + i];
+                    auto p_pairs = [&](auto with_mask) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int q = 32 * c + 2 * i;
-                        const uint64_t nlq = (i & 1) ? nl[i >> 1].y : nl[i >> 1].x;
-                        const float2 x = f2_unpack(
-                            ffma2(f2_pack(u2f(sv[2 * i]), u2f(sv[2 * i + 1])), c2, nlq));
-                        float p0 = ex2(x.x);
-                        float p1 = ex2(x.y);
-                        if (diag) {
-                            if (kg > qh + q) p0 = 0.f;
-                            if (kg > qh + q + 1) p1 = 0.f;
-                        }
-                        if constexpr (LOCAL) {
-                            if (wedge) {
-                                if (qh + q >= kg + window) p0 = 0.f;
-                                if (qh + q + 1 >= kg + window) p1 = 0.f;
+                        for (int i = 0; i < 16; ++i) {
+                            const int q = 32 * c + 2 * i;
+                            const uint64_t nlq = (i & 1) ? nl[i >> 1].y : nl[i >> 1].x;
+                            const float2 x = f2_unpack(
+                                ffma2(f2_pack(u2f(sv[2 * i]), u2f(sv[2 * i + 1])), c2, nlq));
+                            float p0 = ex2(x.x);
+                            float p1 = ex2(x.y);
+                            if constexpr (decltype(with_mask)::value) {
+                                if (diag) {
+                                    if (kg > qh + q) p0 = 0.f;
+                                    if (kg > qh + q + 1) p1 = 0.f;
+                                }
+                                if constexpr (LOCAL) {
+                                    if (wedge) {
+                                        if (qh + q >= kg + window) p0 = 0.f;
+                                        if (qh + q + 1 >= kg + window) p1 = 0.f;
+                                    }
+                                }
+                                if (kg >= N) p0 = p1 = 0.f;  // key row past a ragged end
                             }
+                            pk[i] = pack_bf16(p0, p1);
                         }
-                        if (kg >= N) p0 = p1 = 0.f;  // key row past a ragged end
-                        pk[i] = pack_bf16(p0, p1);
-                    }
+                    };
+                    if (masked) p_pairs(std::true_type{});
+                    else p_pairs(std::false_type{});
                     tmem_st16(tS + 16 * c, pk);
                     if (c == 0) {
 #pragma unroll
