@@ -571,10 +571,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const uint64_t ndq = (i & 1) ? nd[i >> 1].y : nd[i >> 1].x;
-                        const uint64_t pp = f2_pack(u2f(pk[i] << 16), u2f(pk[i] & 0xffff0000u));
-                        const uint64_t t = fadd2(f2_pack(u2f(dp[2 * i]), u2f(dp[2 * i + 1])), ndq);
-                        const float2 d = f2_unpack(fmul2(pp, t));
-                        ds[i] = pack_bf16(d.x, d.y);
+                        // dP - D in fp32, rounded to bf16, times the bf16 P
+                        const float2 t = f2_unpack(
+                            fadd2(f2_pack(u2f(dp[2 * i]), u2f(dp[2 * i + 1])), ndq));
+                        ds[i] = mul_bf16x2(pk[i], pack_bf16(t.x, t.y));
                     }
                     tmem_st16(tDP + 16 * c, ds);
 #pragma unroll

@@ -507,6 +507,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return r;
 }
 
+// Lane-wise product of two bf16x2 values, rounded to nearest even.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // ----------------------------------------------- paired fp32 arithmetic ----
 // sm_100+ executes one f32x2 instruction for two fp32 lanes held in a 64-bit
 // register pair (element 0 in the low half).
