@@ -253,9 +253,9 @@ class HostPipeline:
                  for n in ("q", "k", "v", "do", "o", "dq", "dk", "dv")}
             t["lse"] = torch.empty((B, H, N), dtype=torch.float32, device=self.device)
             t["ws"] = torch.empty(ws_bytes, dtype=torch.uint8, device=self.device)
-            t["free"] = torch.cuda.Event()   # outputs copied out: the set may be refilled
-            t["loaded"] = torch.cuda.Event()
-            t["done"] = torch.cuda.Event()
+            t["loaded"] = torch.cuda.Event()  # inputs copied in
+            t["done"] = torch.cuda.Event()    # kernels finished: the inputs may be refilled
+            t["free"] = torch.cuda.Event()    # outputs copied out: they may be rewritten
             self.bufs.append(t)
         self.k = 0
 
@@ -263,12 +263,16 @@ class HostPipeline:
         b = self.bufs[self.k % len(self.bufs)]
         self.k += 1
         compute = torch.cuda.current_stream(self.device)
+        # the set's inputs are refilled once its previous step's kernels are done
+        # (not its copies out, which read only the outputs), and the kernels
+        # rewrite the outputs once those have been copied out
         with torch.cuda.stream(self.h2d):
-            self.h2d.wait_event(b["free"])
+            self.h2d.wait_event(b["done"])
             for n, src in (("q", q), ("k", k), ("v", v), ("do", do)):
                 b[n].copy_(src, non_blocking=True)
             b["loaded"].record(self.h2d)
         compute.wait_event(b["loaded"])
+        compute.wait_event(b["free"])
         fwd(b["q"], b["k"], b["v"], self.causal, self.tau, out=b["o"], lse=b["lse"])
         bwd(b["q"], b["k"], b["v"], b["o"], b["do"], b["lse"], self.causal, self.tau,
             dq=b["dq"], dk=b["dk"], dv=b["dv"], workspace=b["ws"])
