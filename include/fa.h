@@ -88,6 +88,10 @@ FA_API size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  * by the caller and free for the duration of the call on this stream; NULL
  * asks the library to take it with cudaMallocAsync on the stream and give it
  * back with cudaFreeAsync after the last kernel.
+ * Arithmetic: S, dP and every product accumulate in fp32. P and dS enter the
+ * tensor-core products as bf16. dS is the bf16 product of the bf16 P and
+ * dP - D, which is formed in fp32 and rounded to bf16. dQ is summed over the
+ * key tiles in an fp32 accumulator in the workspace.
  * Source: tonho.wtf "flash attention", section "como funciona", backward
  * paragraph (keep O and the statistics, rebuild S and P, D_i = dO_i . O_i);
  * "FlashAttention: O Que E e Como Acelera LLMs na Pratica", pillar 2
