@@ -476,12 +476,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             const ulonglong2* nl4 = reinterpret_cast<const ulonglong2*>(lse2_s + st * 128 + kQC * h);
             ulonglong2 nl0[8];
             uint32_t pkeep[16];  // the first chunk's packed P^T, reused by dS^T below
-            if (ok) ok = __all_sync(FULL, mbar_wait(bar_qf + 8 * st, (s >> 1) & 1, wd, kSiteDsQ));
+            if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_qf + 8 * st, (s >> 1) & 1, wd, kSiteDsQ));
             if (ok) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) nl0[i] = nl4[i];
             }
-            if (ok) ok = __all_sync(FULL, mbar_wait(bar_s, s & 1, wd, kSiteDsS));
+            if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_s, s & 1, wd, kSiteDsS));
             if (ok) {
                 tc_fence_after();
                 const bool diag = CAUSAL && (q_start == kv_start);
@@ -548,8 +548,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
                 for (int i = 0; i < 8; ++i) nd0[i] = nd4[i];
             }
-            if (ok) ok = __all_sync(FULL, mbar_wait(bar_dp, s & 1, wd, kSiteDsDP) &&
-                                              (s == 0 || mbar_wait(bar_dq, (s - 1) & 1, wd, kSiteDsDQ)));
+            if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_dp, s & 1, wd, kSiteDsDP) &&
+                                              (s == 0 || mbar_wait_sleep(bar_dq, (s - 1) & 1, wd, kSiteDsDQ)));
             if (ok) {
                 tc_fence_after();
 #pragma unroll
@@ -591,7 +591,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             mbar_arrive(bar_ds);
 
             // dQ drain: this warpgroup's D/2 columns -> fp32 tiles -> bulk reduce-add
-            if (ok) ok = __all_sync(FULL, mbar_wait(bar_dq, s & 1, wd, kSiteDrain));
+            if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_dq, s & 1, wd, kSiteDrain));
             uint8_t* stage = smem + L::kStage0 + st * L::kStageBytes;
             uint32_t acc[kDrainBoxes][32];
             if (ok) {
@@ -604,7 +604,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 mbar_arrive(bar_dr);
                 // stage fp32 boxes of [128 x 32] over this step's Q (warpgroup 0) and dO
                 // (warpgroup 1): dO is free (dV, dP^T done before dQ), Q once dK is
-                if (h < NWG / 2) ok = __all_sync(FULL, mbar_wait(bar_dk, s & 1, wd, kSiteDrain));
+                if (h < NWG / 2) ok = __all_sync(FULL, mbar_wait_sleep(bar_dk, s & 1, wd, kSiteDrain));
             } else {
                 mbar_arrive(bar_dr);
             }
@@ -626,7 +626,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         // and V tiles, which no MMA reads any more: the commit after the last dK
         // covers every MMA of this CTA (warpgroup 1 has not waited for it yet)
         if (ok && n_steps > 0)
-            ok = __all_sync(FULL, mbar_wait(bar_dk, (n_steps - 1) & 1, wd, kSiteDrain));
+            ok = __all_sync(FULL, mbar_wait_sleep(bar_dk, (n_steps - 1) & 1, wd, kSiteDrain));
         if (ok) {
             tc_fence_after();
             const uint32_t tDV = tmem + lane_off + L::kTmDV, tDK = tmem + lane_off + L::kTmDK;

@@ -100,6 +100,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` for the phase.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Error word layout (one 32-bit word in global memory per library instance):
 // bit 0 = some wait timed out; bits 8..15 = the first wait site that did.
 struct Watchdog {
@@ -118,6 +133,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     uint32_t n = 0;
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((++n & 31u) == 0u) {
+            if (*wd.abort_cta) return false;
+            if (globaltimer_ns() - t0 > wd.limit_ns) {
+                *wd.abort_cta = 1;
+                atomicCAS(wd.err, 0u, 1u | ((site & 0xffu) << 8));
+                return false;
+            }
+        }
+    }
+}
+
+// mbar_wait for warps with nothing else to issue: each poll may sleep up to
+// 20 us, so a long wait takes fewer of the scheduler's issue slots.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const Watchdog& wd,
+                                                uint32_t site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t n = 0;
+    while (true) {
+        if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
         if ((++n & 31u) == 0u) {
             if (*wd.abort_cta) return false;
             if (globaltimer_ns() - t0 > wd.limit_ns) {
