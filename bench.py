@@ -31,6 +31,8 @@ if ROOT not in sys.path:
 METRIC = ("attention fwd and fwd+bwd TFLOP/s (bf16, causal) and % of GB300 dense BF16 peak")
 DEFAULT_WORKLOAD = "long_sink_b1h16_n16384_d128_causal"
 L2_FLUSH_BYTES = 512 << 20          # > the 129 MB L2, written between timed steps
+ISSUE_FLOP_PER_CLK_SM = 8192        # dense bf16 tcgen05 rate per SM per clock (measured)
+NUM_SMS = 152
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -119,14 +121,16 @@ class ClockSampler:
     FIELDS = "timestamp," + CLOCK_FIELDS
     REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, index: int, period_ms: int = 50):
-        self.index, self.period_ms, self.proc, self.path = index, period_ms, None, None
+    def __init__(self, index: int, period_ms: int = 50, path=None):
+        self.index, self.period_ms, self.proc, self.path = index, period_ms, None, path
         self.t_start = self.t_end = None
+        self.tmpdir = None
 
     def __enter__(self):
-        out_dir = os.path.join(ROOT, "gpurun_out")
-        os.makedirs(out_dir, exist_ok=True)
-        self.path = os.path.join(out_dir, f"clocks_gpu{self.index}.csv")
+        if self.path is None:      # a private temporary file unless --clock-csv names one
+            import tempfile
+            self.tmpdir = tempfile.mkdtemp(prefix="fa_clocks_")
+            self.path = os.path.join(self.tmpdir, f"clocks_gpu{self.index}.csv")
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
@@ -153,6 +157,13 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
             self.fh.close()
+
+    def cleanup(self):
+        """Remove the temporary CSV (after summary())."""
+        if self.tmpdir is not None:
+            import shutil
+            shutil.rmtree(self.tmpdir, ignore_errors=True)
+            self.tmpdir = None
 
     @staticmethod
     def _parse_time(ts: str):
@@ -255,7 +266,7 @@ def run_ours(args):
         e.record(stream)           # materialise the handles
     torch.cuda.synchronize(dev)
 
-    with ClockSampler(local) as clocks:
+    with ClockSampler(local, path=args.clock_csv) as clocks:
         barrier(world, dev)
         torch.cuda.synchronize(dev)
         clocks.mark_start()
@@ -299,6 +310,18 @@ def run_ours(args):
                 "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)",
                 "traffic": profiled_traffic(dom_name)}
 
+    clk = clocks.summary()
+    clocks.cleanup()
+    # the tensor pipe's issue-rate ceiling at the clock seen during the timed steps:
+    # 8192 dense bf16 FLOP per clock per SM (a 128x128x16 MMA every 64 cycles, measured)
+    sm_mhz = clk.get("sm_mhz") or clk.get("sm_max_mhz") or 2070.0
+    issue_ceiling = ISSUE_FLOP_PER_CLK_SM * NUM_SMS * sm_mhz * 1e6 / 1e12
+    roofline["issue_ceiling_tflops"] = round(issue_ceiling, 1)
+    roofline["frac_of_issue_ceiling"] = round(dom_tf / issue_ceiling, 4)
+    roofline["issue_ceiling_source"] = (f"{ISSUE_FLOP_PER_CLK_SM} FLOP/clk/SM x {NUM_SMS} SMs x "
+                                        f"median SM clock {sm_mhz:.0f} MHz in the timed steps")
+
+    configs_leg = measure_configs(w, dev, min(args.steps, 20), peak) if args.configs else None
     window_leg = (measure_window(w, q, k, v, do, dev, args.window, min(args.steps, 20), peak)
                   if args.window > 0 and w.causal else None)
     blocks_leg = (measure_blocks(w, q, k, v, do, dev, min(args.steps, 20), peak)
@@ -333,6 +356,7 @@ def run_ours(args):
                             "frac": round(bwdk_tf / peak, 4)},
         "fwd_bwd_step": {"ms": round(step_avg_ms, 4), "tflops_per_gpu": round(value / world, 2)},
         "roofline": roofline,
+        "configs": configs_leg,
         "sliding_window": window_leg,
         "block_sparse": blocks_leg,
         "decode": decode_leg,
@@ -340,13 +364,85 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 4 * args.steps,
-        "clocks": clocks.summary(),
+        "clocks": clk,
         "wall_s_timed_loop": round(wall, 3),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def measure_configs(headline, dev, steps, peak):
+    """Every other named workload (the tiny check, the two GPT-2 shapes and the
+    128k forward-only one), timed like the headline: L2 flushed before each
+    step, CUDA events around the forward kernel, the backward main kernel and
+    the whole fa_fwd + fa_bwd step (pre and post kernels included)."""
+    import torch
+    from exact_io_aware_12_gb300 import api, _lib
+    from exact_io_aware_12_gb300.workloads import WORKLOADS, flops_fwd, flops_bwd, make_inputs
+
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    out = {}
+    for w in WORKLOADS:
+        if w.name == headline.name:
+            continue
+        B, H, N, d = w.shape
+        x = make_inputs(w)
+        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+        do = x["do"].to(dev) if w.backward else None
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        if w.backward:
+            dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+            ws = torch.empty(api.workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+
+        def run(i=None, ev=None):
+            if ev is not None:
+                ev[0].record(stream)
+                _lib.check(_lib.fa_set_timing_events(ev[1].cuda_event, ev[2].cuda_event), "timing")
+            api.fwd(q, k, v, w.causal, w.tau, out=o, lse=lse)
+            if w.backward:
+                if ev is not None:
+                    _lib.check(_lib.fa_set_timing_events(ev[3].cuda_event, ev[4].cuda_event), "timing")
+                api.bwd(q, k, v, o, do, lse, w.causal, w.tau, dq=dq, dk=dk, dv=dv, workspace=ws)
+            if ev is not None:
+                _lib.check(_lib.fa_set_timing_events(None, None), "timing")
+                ev[5].record(stream)
+
+        for _ in range(3):
+            run()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+        for e in sum(ev, []):
+            e.record(stream)
+        torch.cuda.synchronize(dev)
+        for i in range(steps):
+            flush.fill_(float(i))
+            run(i, ev[i])
+        torch.cuda.synchronize(dev)
+        if api.last_device_error(dev) != _lib.FA_OK:
+            raise RuntimeError(f"kernel watchdog fired in the {w.name} leg")
+        ff, fb = flops_fwd(B, H, N, d, w.causal), flops_bwd(B, H, N, d, w.causal)
+        fms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+        sms = sum(e[0].elapsed_time(e[5]) for e in ev) / steps
+        ent = {"B": B, "H": H, "N": N, "d": d, "causal": w.causal, "steps": steps,
+               "fwd": {"ms": round(fms, 4), "tflops": round(ff / fms / 1e9, 2),
+                       "frac": round(ff / fms / 1e9 / peak, 4)}}
+        if w.backward:
+            bms = sum(e[3].elapsed_time(e[4]) for e in ev) / steps
+            ent["bwd_main_kernel"] = {"ms": round(bms, 4), "tflops": round(fb / bms / 1e9, 2),
+                                      "frac": round(fb / bms / 1e9 / peak, 4)}
+            ent["fwd_bwd_step"] = {"ms": round(sms, 4), "tflops": round((ff + fb) / sms / 1e9, 2),
+                                   "frac": round((ff + fb) / sms / 1e9 / peak, 4)}
+        else:
+            ent["step"] = "fa_fwd only (the workload has no backward)"
+        out[w.name] = ent
+        del q, k, v, do, o, lse, x
+        if w.backward:
+            del dq, dk, dv, ws
+        torch.cuda.empty_cache()
+    return out
 
 
 def window_flops_fwd(B, H, N, d, window):
@@ -746,6 +842,10 @@ def main(argv=None):
     ap.add_argument("--no-decode", dest="decode", action="store_false",
                     help="skip the decode leg")
     ap.add_argument("--no-fp8", dest="fp8", action="store_false", help="skip the FP8 leg")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="skip timing the other named workloads")
+    ap.add_argument("--clock-csv", default=None,
+                    help="keep the nvidia-smi clock samples in this file (default: a temp file)")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: forward/backward TFLOP/s over d, causal and N")
     ap.add_argument("--decode-shape", default="8,16,1,32768,128",

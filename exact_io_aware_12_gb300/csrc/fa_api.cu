@@ -538,29 +538,26 @@ fa_status fa_watchdog_selftest(unsigned long long limit_ns, void* stream) {
 static __device__ __align__(256) unsigned char g_fa_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
 
 namespace {
-struct NoAllocScratch {
-    std::once_flag once;
-    void* ptr = nullptr;  // device address on this device, or null if the lookup failed
-};
-NoAllocScratch g_noalloc[fa::kMaxDevices];
+// The scratch array's device address, per device; null until a lookup succeeds.
+// A failed lookup (for instance a first call made while the stream is being
+// captured) is not remembered: the next call tries again.
+std::atomic<void*> g_noalloc_ptr[fa::kMaxDevices];
 
-// Runs once per device, with that device current (the caller's current device).
+// Looks the array's address up on the current device (the caller's).
 void* noalloc_scratch_for_current_device() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= fa::kMaxDevices) {
         cudaGetLastError();
         return nullptr;
     }
-    NoAllocScratch& ns = g_noalloc[dev];
-    std::call_once(ns.once, [&ns] {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_fa_noalloc_scratch) == cudaSuccess) {
-            ns.ptr = p;
-        } else {
-            cudaGetLastError();
-        }
-    });
-    return ns.ptr;
+    void* p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (p != nullptr) return p;
+    if (cudaGetSymbolAddress(&p, g_fa_noalloc_scratch) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    g_noalloc_ptr[dev].store(p, std::memory_order_release);
+    return p;
 }
 }  // namespace
 
@@ -573,6 +570,9 @@ extern "C" fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V,
     if (s != FA_OK || empty) return s;
     // the one limit of this entry point: the problem's scratch must fit the array
     if (fa_bwd_workspace_size(B, H, N, d) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+    // an unsupported device gets the same answer as from every other entry point
+    fa_status why = FA_OK;
+    if (fa::current_device(&why) == nullptr) return why;
     void* scratch = noalloc_scratch_for_current_device();
     if (scratch == nullptr) return FA_ERR_CUDA;
     // fa_bwd with a caller-provided workspace allocates nothing

@@ -259,9 +259,11 @@ FA_API fa_status fa_set_timing_events(void* start, void* stop);
  * the call returns FA_ERR_WORKSPACE before doing anything.  The call makes no
  * cudaMalloc/cudaFree (or any other allocating) call.
  *
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture begins.  All calls share the one array and it keeps the previous
+ * The first call on a device looks up the array's device address (with that
+ * device current) and keeps it; make that first call before any stream
+ * capture begins.  A lookup that fails returns FA_ERR_CUDA and is retried on
+ * the next call.  On a device other than sm_103 the call returns
+ * FA_ERR_UNSUPPORTED, as every other entry point does.  All calls share the one array and it keeps the previous
  * call's contents (the kernels clear what must start at zero), so two calls
  * whose work overlaps on the GPU (different streams, or different host
  * threads, on the same device) race on it and give wrong results: order them.

@@ -142,3 +142,19 @@ def test_product_and_oracle_share_no_code():
             text = open(os.path.join(ROOT, "oracle", f)).read()
             assert not re.search(r"^\s*(import|from)\s+exact_io_aware_12_gb300", text, re.M), f
             assert "#include \"" not in text and "csrc" not in text, f
+
+
+def _header_define(name):
+    """Value of an integer #define in include/fa.h (products of unsigned literals)."""
+    m = re.search(rf"#define\s+{name}\s+\(?([0-9u\s*]+)\)?", open(HEADER).read())
+    assert m, name
+    value = 1
+    for factor in m.group(1).split("*"):
+        value *= int(factor.strip().rstrip("u"))
+    return value
+
+
+def test_python_constants_match_the_header():
+    assert _lib.NOALLOC_SCRATCH_BYTES == _header_define("FA_NOALLOC_SCRATCH_BYTES")
+    assert _lib.BLOCK_MASK_EDGE == _header_define("FA_BLOCK_MASK_EDGE")
+    assert _lib.BLOCK_MASK_MAX_N == _header_define("FA_BLOCK_MASK_MAX_N")
