@@ -17,10 +17,11 @@
 //               P^T  = exp2(c S^T - log2e LSE_i)   elementwise warps, written
 //                                         back to tensor memory as bf16 over S^T
 //               dV  += P^T dO_i           tcgen05, A read from tensor memory
-//               dS^T = P^T o (dP^T - D_i) elementwise warps, to tensor memory
-//                                         (over dP^T) and to smem
-//               dK  += dS^T Q_i           tcgen05, A from tensor memory
-//               dQ_i = dS K               tcgen05, A = dS^T from smem
+//               dS^T = P^T o (dP^T - D_i) elementwise warps, to smem (and at
+//                                         d = 128 to tensor memory beside P^T)
+//               dQ_i = dS K               tcgen05, A = dS^T from smem (MN-major)
+//               dK  += dS^T Q_i           tcgen05, A from tensor memory (d = 128)
+//                                         or the smem tile (d = 64)
 //             the elementwise warps (NWG warpgroups: four at d = 128, two at
 //             d = 64, each a share of the query columns) also read dQ_i out of
 //             tensor memory into fp32 smem tiles that the reducer warp adds
@@ -29,8 +30,12 @@
 //             loader warp issues the TMA copies, the MMA warp the MMAs.
 //   bwd_post  dQ = bf16(tau * accumulator).
 // Tensor memory (512 columns): dV and dK accumulators (d each), S^T (128),
-// dP^T (128); for d = 128 the dQ tile reuses the S^T columns once P^T has
-// been consumed, so the next S^T waits until dQ has been read out.
+// dP^T (128).  P^T (bf16, two per column) is written over the first half of
+// each warpgroup's S^T columns, and at d = 128 dS^T over the second half, so
+// the dV (and at d = 128 the dK) MMA reads its A operand from tensor memory;
+// the next S^T goes out right after dK.  For d = 128 the dQ tile reuses the
+// dP^T columns once dS^T has been formed, so the next dP^T waits until dQ has
+// been read out.  For d = 64, dQ has 64 columns of its own.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -68,8 +73,13 @@ struct BwdLayout {
     static constexpr int kBytes = kBars + 512;
     // tensor-memory columns
     static constexpr uint32_t kTmDV = 0, kTmDK = D, kTmS = 2 * D, kTmDP = 2 * D + 128;
-    static constexpr bool kDQAliasS = (D == 128);
-    static constexpr uint32_t kTmDQ = kDQAliasS ? kTmS : 2 * D + 256;
+    static constexpr bool kDQAliasDP = (D == 128);
+    // dK's A operand: dS^T from tensor memory (beside P^T) at d = 128, where it
+    // saves the shared-memory reads of an SS MMA; from the smem dS^T tile at
+    // d = 64, where the extra tensor-memory store costs the elementwise phase
+    // more than it saves
+    static constexpr bool kDSInTmem = (D == 128);
+    static constexpr uint32_t kTmDQ = kDQAliasDP ? kTmDP : 2 * D + 256;
 };
 
 struct BwdBarriers {
@@ -104,6 +114,7 @@ struct BwdParams {
     unsigned long long wait_limit_ns;
     const uint8_t* blocks;          // block mask [heads][n_kv][n_kv] (kMaskBlocks)
     long long blocks_head_stride;   // bytes between heads' masks (0: one mask)
+    int head_group;                 // heads whose key tiles are interleaved in launch order
 };
 
 enum : uint32_t {
@@ -146,6 +157,20 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uin
                        b_lo + ((k * 2048) >> 4), kDescHi, id);
 }
 
+// D (+)= A B with A a K-major smem tile [128 rows(M) x 128(K)] (two 64-column
+// boxes) and B an MN-major smem tile [128 rows(K) x Dn].
+template <int Dn>
+__device__ __forceinline__ void mma_rows_mn(uint32_t tmem_d, uint32_t a_lo, uint32_t b_lo,
+                                            bool accumulate) {
+    constexpr uint32_t id = idesc_bf16(128, Dn, false, true);
+    if (accumulate) mma_ss_warp<1>(tmem_d, a_lo, b_lo, kDescHi, id);
+    else mma_ss_warp<0>(tmem_d, a_lo, b_lo, kDescHi, id);
+#pragma unroll
+    for (int k = 1; k < 128 / 16; ++k)
+        mma_ss_warp<1>(tmem_d, a_lo + (((k / 4) * (128 * 128) + (k % 4) * 32) >> 4),
+                       b_lo + ((k * 2048) >> 4), kDescHi, id);
+}
+
 // D = A B with A MN-major [128(K) x 128(M)] and B MN-major [128(K) x Dn].
 template <int Dn>
 __device__ __forceinline__ void mma_mn_mn(uint32_t tmem_d, uint32_t a_lo, uint32_t b_lo) {
@@ -182,8 +207,20 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int kv_tile = blockIdx.y;  // tile 0 has the most query tiles when causal
+    // Launch order (x fastest) walks groups of p.head_group heads; inside a group
+    // the key tiles go in order (tile 0 has the most query tiles when causal),
+    // the group's heads interleaved.  So the CTAs resident at one time work on
+    // a few heads, whose Q, dO and fp32 dQ accumulator stay in L2.
+    int bh, kv_tile;
+    {
+        const long long i = blockIdx.x + static_cast<long long>(gridDim.x) * blockIdx.y;
+        const long long per_group = static_cast<long long>(p.head_group) * gridDim.y;
+        const int g = static_cast<int>(i / per_group);
+        const int j = static_cast<int>(i - g * per_group);
+        const int heads = min(p.head_group, static_cast<int>(gridDim.x) - g * p.head_group);
+        kv_tile = j / heads;
+        bh = g * p.head_group + (j - kv_tile * heads);
+    }
     const int N = p.N;
     const int kv_start = kv_tile * kBK;
     const int n_q = (N + kBQ - 1) / kBQ;
@@ -336,6 +373,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             const uint32_t k_mn = sw128_desc_lo(sbase + L::kK, kLboMN);
             const uint32_t v_lo = sw128_desc_lo(sbase + L::kV, 16);
             const uint32_t ds_mn = sw128_desc_lo(sbase + L::kDS, kLboMN);
+            const uint32_t ds_lo = sw128_desc_lo(sbase + L::kDS, 16);
             const uint32_t q_lo0 = sw128_desc_lo(sbase + L::kStage0, 16);
             const uint32_t q_mn0 = sw128_desc_lo(sbase + L::kStage0, kLboMN);
             const uint32_t do_lo0 = sw128_desc_lo(sbase + L::kStage0 + L::kTile, 16);
@@ -364,16 +402,20 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 mma_commit_warp(bar_de + 8 * st);  // the last MMA that reads this dO
                 if (!__all_sync(0xffffffffu, mbar_wait(bar_ds, s & 1, wd, kSiteMmaDS))) { ok = false; break; }
                 tc_fence_after();
-                // dQ before dK: its drain (and so the next S^T over its columns)
-                // can start while dK runs
-                if (!L::kDQAliasS && s > 0) {
+                // d = 64: the dQ columns are reused every step
+                if (!L::kDQAliasDP && s > 0) {
                     if (!__all_sync(0xffffffffu, mbar_wait(bar_dr, (s - 1) & 1, wd, kSiteMmaDrain))) { ok = false; break; }
                     tc_fence_after();
                 }
+                // dQ first: its drain is on the elementwise warps' path; dK and the
+                // next S^T run while they drain it
                 mma_mn_mn<D>(tmem + L::kTmDQ, ds_mn, k_mn);                            // dQ
                 mma_commit_warp(bar_dq);
-                mma_tmem_a<D, kQC>(tmem + L::kTmDK, tmem + L::kTmDP, q_mn0 + so, s > 0);   // dK
-                mma_commit_warp(bar_dk);
+                if constexpr (L::kDSInTmem)
+                    mma_tmem_a<D, kQC>(tmem + L::kTmDK, tmem + L::kTmS + kQC / 2, q_mn0 + so, s > 0);  // dK
+                else
+                    mma_rows_mn<D>(tmem + L::kTmDK, ds_lo, q_mn0 + so, s > 0);           // dK
+                mma_commit_warp(bar_dk);           // d = 64: also, the dS^T tile is free again
                 mma_commit_warp(bar_qe + 8 * st);
                 if (s + 1 < n_steps) {
                     const int st1 = (s + 1) & 1;
@@ -383,14 +425,15 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                         break;
                     }
                     tc_fence_after();
-                    // S^T first: the next step's P^T work waits on it, while dP^T
-                    // is needed only later (the tensor pipe runs in issue order)
-                    if (L::kDQAliasS) {
+                    // S^T over P^T and dS^T, which only the dV and dK MMAs above
+                    // read (the tensor pipe runs in issue order)
+                    mma_rows_rows<D>(tmem + L::kTmS, k_lo, q_lo0 + so1);     // S^T next
+                    mma_commit_warp(bar_s);
+                    // d = 128: dP^T over the dQ tile, once it has been read out
+                    if (L::kDQAliasDP) {
                         if (!__all_sync(0xffffffffu, mbar_wait(bar_dr, s & 1, wd, kSiteMmaDrain))) { ok = false; break; }
                         tc_fence_after();
                     }
-                    mma_rows_rows<D>(tmem + L::kTmS, k_lo, q_lo0 + so1);     // S^T next
-                    mma_commit_warp(bar_s);
                     if (!__all_sync(0xffffffffu, mbar_wait(bar_df + 8 * st1, ((s + 1) >> 1) & 1, wd, kSiteMmaQ))) {
                         ok = false;
                         break;
@@ -539,7 +582,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             }
             mbar_arrive(bar_p);
 
-            // dS^T = P^T o (dP^T - D), to tensor memory (over dP^T) and to smem.
+            // dS^T = P^T o (dP^T - D), to the smem tile that the dQ MMA reads (and at
+            // d = 64 the dK MMA), once the MMAs of the previous step are done with
+            // it, and at d = 128 also to tensor memory beside P^T (dK's A operand).
             // -D per query, pairs of adjacent queries as one 64-bit value (16-byte
             // loads); the first chunk's are read before the wait for dP^T
             const ulonglong2* nd4 = reinterpret_cast<const ulonglong2*>(dvec_s + st * 128 + kQC * h);
@@ -549,7 +594,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 for (int i = 0; i < 8; ++i) nd0[i] = nd4[i];
             }
             if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_dp, s & 1, wd, kSiteDsDP) &&
-                                              (s == 0 || mbar_wait_sleep(bar_dq, (s - 1) & 1, wd, kSiteDsDQ)));
+                                              (s == 0 || mbar_wait_sleep(L::kDSInTmem ? bar_dq : bar_dk, (s - 1) & 1, wd,
+                                                                         kSiteDsDQ)));
             if (ok) {
                 tc_fence_after();
 #pragma unroll
@@ -576,7 +622,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                             fadd2(f2_pack(u2f(dp[2 * i]), u2f(dp[2 * i + 1])), ndq));
                         ds[i] = mul_bf16x2(pk[i], pack_bf16(t.x, t.y));
                     }
-                    tmem_st16(tDP + 16 * c, ds);
+                    if constexpr (L::kDSInTmem) tmem_st16(tS + kQC / 2 + 16 * c, ds);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         const int chunk = ds_chunk0 + 4 * c + q4;
@@ -585,7 +631,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     }
                 }
                 fence_async_shared();
-                tmem_st_wait();
+                if constexpr (L::kDSInTmem) tmem_st_wait();
                 tc_fence_before();
             }
             mbar_arrive(bar_ds);
@@ -730,6 +776,18 @@ __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restric
     }
 }
 
+// Heads per launch-order group: as many as keep their Q, dO, K, V (bf16) and
+// fp32 dQ accumulator within about half of L2, and at most 16 (measured on
+// GB300: at N = 16384, d = 128 two heads per group beat all 16 by 3-6% and
+// cut the backward's DRAM traffic ~4x; short GPT-2-sized problems do best
+// with 16).
+int bwd_head_group(int BH, int N, int D) {
+    constexpr double kL2Share = 64.0 * 1024 * 1024;
+    const double per_head = static_cast<double>(N) * D * (4 * 2 + 4);
+    const int g = static_cast<int>(kL2Share / per_head);
+    return max(1, min(min(BH, 16), g));
+}
+
 template <int D, bool CAUSAL, int MASK = kMaskNone>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     using L = BwdLayout<D>;
@@ -772,6 +830,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         p.window = (a.window > 0 && a.window < a.N) ? a.window : 0;
         p.blocks = a.blocks;
         p.blocks_head_stride = a.blocks_head_stride;
+        p.head_group = bwd_head_group(a.BH, a.N, D);
         p.err = a.err;
         p.wait_limit_ns = a.wait_limit_ns;
         dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(p.n_kv));
