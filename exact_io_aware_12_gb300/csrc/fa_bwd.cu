@@ -776,16 +776,20 @@ __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restric
     }
 }
 
-// Heads per launch-order group: as many as keep their Q, dO, K, V (bf16) and
-// fp32 dQ accumulator within about half of L2, and at most 16 (measured on
-// GB300: at N = 16384, d = 128 two heads per group beat all 16 by 3-6% and
-// cut the backward's DRAM traffic ~4x; short GPT-2-sized problems do best
-// with 16).
-int bwd_head_group(int BH, int N, int D) {
-    constexpr double kL2Share = 64.0 * 1024 * 1024;
+// Heads per launch-order group (a power of two, at most 16).  Measured on
+// GB300, interleaved runs: causal problems do best with the group's Q, dO, K, V
+// (bf16) and fp32 dQ accumulator near 128 MB (16k tokens, d = 128: 4 heads,
+// 2.04 vs 2.12 ms with all 16 in flight), non-causal ones near 48 MB (1-2
+// heads: 4.13 vs 4.45 ms), GPT-2-sized ones with 16.  A block mask keeps every
+// head in flight: its few heavy key tiles (global anchors) must start first,
+// and grouping left the last group's anchors as a tail (0.31 vs 0.50 ms).
+int bwd_head_group(int BH, int N, int D, bool causal, int mask) {
+    if (mask == kMaskBlocks) return BH;
+    const double budget = (causal ? 128.0 : 48.0) * 1024 * 1024;
     const double per_head = static_cast<double>(N) * D * (4 * 2 + 4);
-    const int g = static_cast<int>(kL2Share / per_head);
-    return max(1, min(min(BH, 16), g));
+    int g = 1;
+    while (g < 16 && 2.0 * g * per_head <= budget) g *= 2;
+    return max(1, min(BH, g));
 }
 
 template <int D, bool CAUSAL, int MASK = kMaskNone>
@@ -830,7 +834,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         p.window = (a.window > 0 && a.window < a.N) ? a.window : 0;
         p.blocks = a.blocks;
         p.blocks_head_stride = a.blocks_head_stride;
-        p.head_group = bwd_head_group(a.BH, a.N, D);
+        p.head_group = bwd_head_group(a.BH, a.N, D, CAUSAL, MASK);
         p.err = a.err;
         p.wait_limit_ns = a.wait_limit_ns;
         dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(p.n_kv));
