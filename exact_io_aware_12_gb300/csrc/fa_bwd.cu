@@ -23,7 +23,7 @@
 //               dK  += dS^T Q_i           tcgen05, A from tensor memory (d = 128)
 //                                         or the smem tile (d = 64)
 //             the elementwise warps (NWG warpgroups: four at d = 128, two at
-//             d = 64, each a share of the query columns) also read dQ_i out of
+//             d = 64, each a share of the query and d columns) also read dQ_i out of
 //             tensor memory into fp32 smem tiles that the reducer warp adds
 //             into the accumulator with TMA bulk reductions (no per-element
 //             atomics); at the end they write dK (scaled by tau) and dV.  The
@@ -192,7 +192,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                    const BwdParams p) {
     using L = BwdLayout<D>;
     static_assert(sizeof(BwdBarriers) <= L::kBytes - L::kBars, "barrier block overflows its slot");
-    static_assert(NWG == 2 || (NWG == 4 && D == 128), "four warpgroups need 32-column drain boxes");
+    static_assert(NWG == 2 || NWG == 4, "two or four elementwise warpgroups");
+    static_assert((D / NWG) % 16 == 0, "each warpgroup drains whole 16-column chunks");
     constexpr int kProducerWarp = 4 * NWG, kMmaWarp = 4 * NWG + 1, kReducerWarp = 4 * NWG + 2;
     constexpr int kQC = 128 / NWG;      // query columns of P^T / dS^T per warpgroup
     constexpr int kDC = D / NWG;        // d-columns of dQ, dK, dV per warpgroup
@@ -501,7 +502,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         // columns, and their first 16-byte chunk in it
         uint8_t* ds_row = smem + L::kDS + (kQC * h / 64) * (128 * 128) + r * 128;
         const int ds_chunk0 = (kQC * h % 64) / 8;
-        constexpr int kDrainBoxes = kDC / 32;  // fp32 boxes of 32 columns per warpgroup
+        constexpr int kDrainChunks = kDC / 16;  // 16-column fp32 chunks of dQ per warpgroup
         bool ok = true;
         int qsp = -1;  // block mask: the query tile of the last step
         for (int s = 0; s < n_steps; ++s) {
@@ -639,28 +640,31 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             // dQ drain: this warpgroup's D/2 columns -> fp32 tiles -> bulk reduce-add
             if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_dq, s & 1, wd, kSiteDrain));
             uint8_t* stage = smem + L::kStage0 + st * L::kStageBytes;
-            uint32_t acc[kDrainBoxes][32];
+            uint32_t acc[kDrainChunks][16];
             if (ok) {
                 tc_fence_after();
 #pragma unroll
-                for (int b = 0; b < kDrainBoxes; ++b) tmem_ld32(tDQ + 32 * b, acc[b]);
+                for (int b = 0; b < kDrainChunks; ++b) tmem_ld16(tDQ + 16 * b, acc[b]);
 #pragma unroll
-                for (int b = 0; b < kDrainBoxes; ++b) tmem_ld_wait(acc[b]);
+                for (int b = 0; b < kDrainChunks; ++b) tmem_ld_wait(acc[b]);
                 tc_fence_before();
                 mbar_arrive(bar_dr);
-                // stage fp32 boxes of [128 x 32] over this step's Q (warpgroup 0) and dO
-                // (warpgroup 1): dO is free (dV, dP^T done before dQ), Q once dK is
+                // stage fp32 boxes of [128 x 32] over this step's Q (the first half of the
+                // warpgroups, dQ columns [0, D/2)) and dO (the second half): dO is free
+                // (dV, dP^T done before dQ), Q once dK is
                 if (h < NWG / 2) ok = __all_sync(FULL, mbar_wait_sleep(bar_dk, s & 1, wd, kSiteDrain));
             } else {
                 mbar_arrive(bar_dr);
             }
             if (ok) {
 #pragma unroll
-                for (int b = 0; b < kDrainBoxes; ++b) {
-                    uint8_t* box = stage + (h * kDrainBoxes + b) * L::kBox + r * 128;
+                for (int b = 0; b < kDrainChunks; ++b) {
+                    // columns h kDC + 16 b ..: box (32 columns) and first 16-byte chunk in it
+                    const int col = h * kDC + 16 * b;
+                    uint8_t* box = stage + (col / 32) * L::kBox + r * 128;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        *reinterpret_cast<uint4*>(box + ((j ^ (r & 7)) << 4)) =
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint4*>(box + ((((col % 32) / 4 + j) ^ (r & 7)) << 4)) =
                             make_uint4(acc[b][4 * j], acc[b][4 * j + 1], acc[b][4 * j + 2],
                                        acc[b][4 * j + 3]);
                 }
@@ -682,19 +686,19 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 const float scale = which ? p.tau : 1.f;
                 const uint32_t src = which ? tDK : tDV;
 #pragma unroll
-                for (int cc = 0; cc < kDC; cc += 32) {
+                for (int cc = 0; cc < kDC; cc += 16) {
                     const int c0 = h * kDC + cc;
-                    uint32_t o[32];
+                    uint32_t o[16];
                     if (!SPARSE || n_steps > 0) {
-                        tmem_ld32(src + c0, o);
+                        tmem_ld16(src + c0, o);
                         tmem_ld_wait(o);
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = 0u;  // no query sees these keys
+                        for (int i = 0; i < 16; ++i) o[i] = 0u;  // no query sees these keys
                     }
                     const int box = c0 / 64;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < 2; ++q) {
                         const int chunk = (c0 % 64) / 8 + q;
                         uint4 v;
                         v.x = pack_bf16(u2f(o[8 * q + 0]) * scale, u2f(o[8 * q + 1]) * scale);
@@ -819,7 +823,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
             !make_tile_map(&tdk, a.dK, BF, 2, D, a.N, a.BH, 64, kBK) ||
             !make_tile_map(&tdv, a.dV, BF, 2, D, a.N, a.BH, 64, kBK))
             return cudaErrorInvalidValue;
-        // d = 128: four elementwise warpgroups (each half the columns of two)
+        // d = 128: four elementwise warpgroups (32 query columns each); d = 64: two
+        // (four measured 4-8% slower there)
         constexpr int NWG = D == 128 ? 4 : 2;
         auto kern = fa_bwd_main_kernel<D, CAUSAL, MASK, NWG>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
