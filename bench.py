@@ -685,10 +685,11 @@ def measure_fp8(w, dev, steps, peak_bf16):
 
 
 def run_e2e(args, w, x, dev, f_step):
-    """Same step through the public API with host buffers (api.HostPipeline):
-    every step copies its pinned host inputs in and its outputs (O, LSE, dQ,
-    dK, dV) back, inside the timing; the copies of neighbouring steps overlap
-    the kernels, two device buffer sets deep."""
+    """Same step through the C ABI with host buffers (the library's native host
+    pipeline, fa_host_pipeline_*, via api.HostPipeline): every step copies its
+    pinned host inputs in and its outputs (O, LSE, dQ, dK, dV) back, inside the
+    timing; the copies of neighbouring steps overlap the kernels, two device
+    buffer sets deep."""
     import torch
     from exact_io_aware_12_gb300 import api
 
@@ -697,7 +698,6 @@ def run_e2e(args, w, x, dev, f_step):
     hin = {n: x[n].pin_memory() for n in ("q", "k", "v", "do")}
     dq_, dk_, dv_, o_ = (torch.empty(w.shape, dtype=torch.bfloat16).pin_memory() for _ in range(4))
     lse_ = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    stream = torch.cuda.current_stream(dev)
 
     # the public API's host-buffer pipeline: each step copies its inputs in and
     # its results out; neighbouring steps' copies overlap each other's kernels
@@ -710,14 +710,13 @@ def run_e2e(args, w, x, dev, f_step):
         step()
     pipe.synchronize()
     barrier(world, dev)
-    s = torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    pipe.h2d.wait_stream(stream)  # the first timed copy starts after the start event
+    s = pipe.mark()     # after the warm-up; the first timed copy starts after it
     for _ in range(args.steps):
         step()
-    e = pipe.finish_event()
+    e = pipe.mark()     # after the last timed step's copies out
     e.synchronize()
     t = reduce_max(s.elapsed_time(e) / 1e3, world, dev)
+    pipe.close()
     h2d = sum(t_.numel() * t_.element_size() for t_ in hin.values())
     d2h = sum(t_.numel() * t_.element_size() for t_ in (o_, lse_, dq_, dk_, dv_))
     return {"value": round(aggregate_value(f_step, args.steps, world, t), 2), "unit": "TFLOP/s",

@@ -43,6 +43,11 @@ SIGNATURES = {
     "fa_fwd_blocks": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _I, _P]),
     "fa_bwd_blocks": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _F, _I,
                            _P, _I, _P]),
+    "fa_host_pipeline_create": (_I, [_I, _I, _I, _I, _F, _I, _I, _P, ctypes.POINTER(_P)]),
+    "fa_host_pipeline_step": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "fa_host_pipeline_mark": (_I, [_P, _P]),
+    "fa_host_pipeline_sync": (_I, [_P]),
+    "fa_host_pipeline_destroy": (_I, [_P]),
 }
 
 # Block-mask geometry (FA_BLOCK_MASK_EDGE, FA_BLOCK_MASK_MAX_N).
@@ -173,3 +178,26 @@ def fa_bwd_noalloc(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, tau, causal, str
 def check(code: int, where: str) -> None:
     if code != FA_OK:
         raise FAError(code, where)
+
+
+def fa_host_pipeline_create(B, H, N, d, tau, causal, depth, stream):
+    """Returns (status, handle)."""
+    h = ctypes.c_void_p()
+    code = _call("fa_host_pipeline_create", B, H, N, d, tau, causal, depth, stream, ctypes.byref(h))
+    return code, h
+
+
+def fa_host_pipeline_step(p, hQ, hK, hV, hdO, hO, hLSE, hdQ, hdK, hdV) -> int:
+    return _call("fa_host_pipeline_step", p, hQ, hK, hV, hdO, hO, hLSE, hdQ, hdK, hdV)
+
+
+def fa_host_pipeline_mark(p, event) -> int:
+    return _call("fa_host_pipeline_mark", p, event)
+
+
+def fa_host_pipeline_sync(p) -> int:
+    return _call("fa_host_pipeline_sync", p)
+
+
+def fa_host_pipeline_destroy(p) -> int:
+    return _call("fa_host_pipeline_destroy", p)

@@ -227,71 +227,66 @@ def attention(q, k, v, causal: bool = False, tau: Optional[float] = None) -> tor
 
 
 class HostPipeline:
-    """Forward + backward steps on tensors that live in pinned host memory.
+    """Forward + backward steps on tensors that live in pinned host memory,
+    through the library's native host pipeline (fa_host_pipeline_* in
+    include/fa.h).
 
     Each step copies its Q, K, V, dO in, runs fwd and bwd, and copies O, LSE,
-    dQ, dK, dV back out.  With ``depth`` device buffer sets (default 2), one
-    stream per copy direction and the compute on the caller's current stream,
-    the copies of neighbouring steps overlap each other's kernels, as a
-    training or serving loop overlaps the next batch's transfer with the
-    current step.  ``step`` only enqueues work; ``synchronize`` waits for all
-    of it.  Host tensors must be pinned, contiguous, of the configured shape
-    (bf16; LSE fp32), and must not be touched until the step has finished."""
+    dQ, dK, dV back out.  The library owns ``depth`` device buffer sets
+    (default 2) and one stream per copy direction; the kernels run on the
+    caller's current stream.  The copies of neighbouring steps overlap each
+    other's kernels, as a training or serving loop overlaps the next batch's
+    transfer with the current step.  ``step`` only enqueues work;
+    ``synchronize`` waits for all of it.  Host tensors must be pinned,
+    contiguous, of the configured shape (bf16; LSE fp32), and must not be
+    touched until the step has finished."""
 
     def __init__(self, B: int, H: int, N: int, d: int, causal: bool, tau: Optional[float] = None,
                  device: Optional[torch.device] = None, depth: int = 2):
         self.shape = (B, H, N, d)
-        self.causal = bool(causal)
         self.tau = 1.0 / math.sqrt(d) if tau is None else float(tau)
         self.device = device or torch.device("cuda", torch.cuda.current_device())
-        self.h2d = torch.cuda.Stream(self.device)
-        self.d2h = torch.cuda.Stream(self.device)
-        ws_bytes = max(workspace_bytes(B, H, N, d), 1)
-        self.bufs = []
-        for _ in range(max(1, depth)):
-            t = {n: torch.empty(self.shape, dtype=torch.bfloat16, device=self.device)
-                 for n in ("q", "k", "v", "do", "o", "dq", "dk", "dv")}
-            t["lse"] = torch.empty((B, H, N), dtype=torch.float32, device=self.device)
-            t["ws"] = torch.empty(ws_bytes, dtype=torch.uint8, device=self.device)
-            t["loaded"] = torch.cuda.Event()  # inputs copied in
-            t["done"] = torch.cuda.Event()    # kernels finished: the inputs may be refilled
-            t["free"] = torch.cuda.Event()    # outputs copied out: they may be rewritten
-            self.bufs.append(t)
-        self.k = 0
+        self.stream = torch.cuda.current_stream(self.device)
+        with torch.cuda.device(self.device):
+            code, self._p = _lib.fa_host_pipeline_create(B, H, N, d, self.tau, int(bool(causal)),
+                                                         int(depth), self.stream.cuda_stream)
+        _lib.check(code, "fa_host_pipeline_create")
+
+    def _check(self, ts, dtype, shape):
+        for t in ts:
+            if t.is_cuda or t.dtype != dtype or tuple(t.shape) != shape or not t.is_contiguous():
+                raise ValueError(f"host tensors must be contiguous CPU {dtype} of shape {shape}")
 
     def step(self, q, k, v, do, o_out, lse_out, dq_out, dk_out, dv_out) -> None:
-        b = self.bufs[self.k % len(self.bufs)]
-        self.k += 1
-        compute = torch.cuda.current_stream(self.device)
-        # the set's inputs are refilled once its previous step's kernels are done
-        # (not its copies out, which read only the outputs), and the kernels
-        # rewrite the outputs once those have been copied out
-        with torch.cuda.stream(self.h2d):
-            self.h2d.wait_event(b["done"])
-            for n, src in (("q", q), ("k", k), ("v", v), ("do", do)):
-                b[n].copy_(src, non_blocking=True)
-            b["loaded"].record(self.h2d)
-        compute.wait_event(b["loaded"])
-        compute.wait_event(b["free"])
-        fwd(b["q"], b["k"], b["v"], self.causal, self.tau, out=b["o"], lse=b["lse"])
-        bwd(b["q"], b["k"], b["v"], b["o"], b["do"], b["lse"], self.causal, self.tau,
-            dq=b["dq"], dk=b["dk"], dv=b["dv"], workspace=b["ws"])
-        b["done"].record(compute)
-        with torch.cuda.stream(self.d2h):
-            self.d2h.wait_event(b["done"])
-            for n, dst in (("o", o_out), ("lse", lse_out), ("dq", dq_out), ("dk", dk_out),
-                           ("dv", dv_out)):
-                dst.copy_(b[n], non_blocking=True)
-            b["free"].record(self.d2h)
+        self._check((q, k, v, do, o_out, dq_out, dk_out, dv_out), torch.bfloat16, self.shape)
+        self._check((lse_out,), torch.float32, self.shape[:3])
+        code = _lib.fa_host_pipeline_step(self._p, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                          do.data_ptr(), o_out.data_ptr(), lse_out.data_ptr(),
+                                          dq_out.data_ptr(), dk_out.data_ptr(), dv_out.data_ptr())
+        _lib.check(code, "fa_host_pipeline_step")
 
-    def finish_event(self) -> torch.cuda.Event:
-        """An event on the caller's current stream that completes when every
-        step enqueued so far, copies included, has finished."""
-        compute = torch.cuda.current_stream(self.device)
-        compute.wait_stream(self.d2h)
+    def mark(self) -> torch.cuda.Event:
+        """A timing event on the kernels' stream after every step enqueued so
+        far, copies included; copies enqueued later start after it."""
         e = torch.cuda.Event(enable_timing=True)
-        e.record(compute)
+        e.record(self.stream)  # materialise the handle
+        _lib.check(_lib.fa_host_pipeline_mark(self._p, e.cuda_event), "fa_host_pipeline_mark")
         return e
 
+    def finish_event(self) -> torch.cuda.Event:
+        return self.mark()
+
     def synchronize(self) -> None:
-        self.finish_event().synchronize()
+        _lib.check(_lib.fa_host_pipeline_sync(self._p), "fa_host_pipeline_sync")
+
+    def close(self) -> None:
+        if getattr(self, "_p", None) is not None and self._p.value:
+            code = _lib.fa_host_pipeline_destroy(self._p)
+            self._p = None
+            _lib.check(code, "fa_host_pipeline_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

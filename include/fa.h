@@ -23,8 +23,10 @@
  *     are equal, so top-left and bottom-right alignment coincide); 0 = no mask.
  *   - tau is the score scale, finite and > 0 (usually 1/sqrt(d)).
  *   - Every pointer is a device pointer (cudaMalloc / PyTorch CUDA memory)
- *     aligned to 16 bytes.  The caller owns every buffer; the library keeps
- *     no device allocation between calls.  Outputs must not overlap inputs.
+ *     aligned to 16 bytes, except the host buffers of fa_host_pipeline_step.
+ *     The caller owns every buffer; apart from a host pipeline object's
+ *     buffers and fa_bwd_noalloc's fixed scratch array, the library keeps no
+ *     device allocation between calls.  Outputs must not overlap inputs.
  *   - stream is a cudaStream_t (NULL = the legacy default stream).  Calls only
  *     enqueue work on it and never synchronise the host.
  *   - Errors are returned, never printed: invalid arguments are caught before
@@ -272,6 +274,47 @@ FA_API fa_status fa_set_timing_events(void* start, void* stop);
 FA_API fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
                                 const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
                                 int B, int H, int N, int d, float tau, int causal, void* stream);
+
+/*
+ * Host-buffer pipeline: forward + backward steps on tensors that live in host
+ * memory.  Not part of the method (the pages describe device-resident
+ * tensors); it is the runtime a caller with host-resident batches uses, and
+ * the library's end-to-end measurement goes through it.
+ *
+ * fa_host_pipeline_create allocates `depth` (1..8) device buffer sets for one
+ * problem shape (Q, K, V, dO, O, LSE, dQ, dK, dV and the backward workspace,
+ * on the current device; the only allocations the library makes on its own,
+ * owned by the object until fa_host_pipeline_destroy) and two copy streams.
+ * The kernels run on `stream` (NULL = the legacy default stream).
+ *
+ * fa_host_pipeline_step enqueues one step and returns: copy hQ, hK, hV, hdO
+ * (host, bf16 [B][H][N][d]) in; fa_fwd and fa_bwd on the next buffer set; copy
+ * O, LSE (fp32 [B][H][N]), dQ, dK, dV out to hO, hLSE, hdQ, hdK, hdV.  Events
+ * order each set's reuse, so with depth >= 2 the copies of neighbouring steps
+ * overlap the kernels.  Host buffers should be page-locked (cudaHostAlloc /
+ * pinned): pageable memory works but its copies do not overlap.  The caller
+ * must not touch a step's host buffers until that step has finished
+ * (fa_host_pipeline_sync, or an event from fa_host_pipeline_mark).
+ *
+ * fa_host_pipeline_mark records `event` (a cudaEvent_t) on `stream` at a point
+ * after everything enqueued so far, copies included, and makes every copy
+ * enqueued later wait for it: two marks bracket whole steps for timing.
+ * fa_host_pipeline_sync blocks the host until all enqueued work is done.
+ * fa_host_pipeline_destroy synchronises, then frees everything (NULL is a
+ * no-op).  An object is not thread-safe; use one per host thread.
+ * Errors: FA_ERR_INVALID_ARG (null pointers, bad sizes or depth),
+ * FA_ERR_UNSUPPORTED (d not 64 or 128), FA_ERR_CUDA (an allocation or CUDA
+ * call failed), and whatever fa_fwd / fa_bwd return.
+ */
+typedef struct fa_host_pipeline fa_host_pipeline;
+FA_API fa_status fa_host_pipeline_create(int B, int H, int N, int d, float tau, int causal,
+                                         int depth, void* stream, fa_host_pipeline** out);
+FA_API fa_status fa_host_pipeline_step(fa_host_pipeline* p, const void* hQ, const void* hK,
+                                       const void* hV, const void* hdO, void* hO, float* hLSE,
+                                       void* hdQ, void* hdK, void* hdV);
+FA_API fa_status fa_host_pipeline_mark(fa_host_pipeline* p, void* event);
+FA_API fa_status fa_host_pipeline_sync(fa_host_pipeline* p);
+FA_API fa_status fa_host_pipeline_destroy(fa_host_pipeline* p);
 
 #ifdef __cplusplus
 }

@@ -158,3 +158,18 @@ def test_python_constants_match_the_header():
     assert _lib.NOALLOC_SCRATCH_BYTES == _header_define("FA_NOALLOC_SCRATCH_BYTES")
     assert _lib.BLOCK_MASK_EDGE == _header_define("FA_BLOCK_MASK_EDGE")
     assert _lib.BLOCK_MASK_MAX_N == _header_define("FA_BLOCK_MASK_MAX_N")
+
+
+def test_host_pipeline_argument_checks():
+    """Rejected before any CUDA call, so these run without a GPU."""
+    for args in [(0, 1, 128, 64, 0.1, 1, 2), (1, 1, 128, 64, 0.1, 1, 0), (1, 1, 128, 64, 0.1, 1, 9),
+                 (1, 1, 128, 64, float("nan"), 1, 2), (1, 1, 128, 64, 0.1, 2, 2)]:
+        code, h = _lib.fa_host_pipeline_create(*args, None)
+        assert code == _lib.FA_ERR_INVALID_ARG and not h.value
+    code, h = _lib.fa_host_pipeline_create(1, 1, 128, 96, 0.1, 1, 2, None)
+    assert code == _lib.FA_ERR_UNSUPPORTED and not h.value
+    assert _lib.fa_host_pipeline_step(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE) == \
+        _lib.FA_ERR_INVALID_ARG
+    assert _lib.fa_host_pipeline_mark(None, None) == _lib.FA_ERR_INVALID_ARG
+    assert _lib.fa_host_pipeline_sync(None) == _lib.FA_ERR_INVALID_ARG
+    assert _lib.fa_host_pipeline_destroy(None) == _lib.FA_OK

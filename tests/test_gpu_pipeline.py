@@ -1,5 +1,6 @@
-"""api.HostPipeline: steps on pinned host tensors, copies overlapped across
-steps, give the same results as the direct device calls."""
+"""The native host pipeline (fa_host_pipeline_*, through api.HostPipeline):
+steps on pinned host tensors, copies overlapped across steps, give the same
+results as the direct device calls; bad arguments are rejected."""
 import math
 
 import pytest
@@ -34,3 +35,19 @@ def test_pipeline_matches_direct_calls(depth):
         assert torch.equal(o["o"], o_ref.cpu()) and torch.equal(o["lse"], l_ref.cpu())
         assert torch.equal(o["dk"], dk.cpu()) and torch.equal(o["dv"], dv.cpu())
         assert (o["dq"].float() - dq.cpu().float()).abs().max().item() <= 1e-2 * max(1.0, dq.abs().max().item())
+
+
+def test_pipeline_rejects_bad_arguments():
+    stream = torch.cuda.current_stream().cuda_stream
+    for args in [(0, 1, 128, 64, 0.1, 1, 2), (1, 1, 128, 64, 0.1, 1, 0), (1, 1, 128, 64, 0.1, 1, 9),
+                 (1, 1, 128, 64, 0.0, 1, 2), (1, 1, 128, 64, 0.1, 2, 2)]:
+        code, h = _lib.fa_host_pipeline_create(*args, stream)
+        assert code == _lib.FA_ERR_INVALID_ARG and not h.value
+    code, h = _lib.fa_host_pipeline_create(1, 1, 128, 96, 0.1, 1, 2, stream)
+    assert code == _lib.FA_ERR_UNSUPPORTED
+    code, h = _lib.fa_host_pipeline_create(1, 1, 128, 64, 0.1, 1, 2, stream)
+    assert code == _lib.FA_OK and h.value
+    assert _lib.fa_host_pipeline_step(h, None, None, None, None, None, None, None, None, None) == \
+        _lib.FA_ERR_INVALID_ARG
+    assert _lib.fa_host_pipeline_destroy(h) == _lib.FA_OK
+    assert _lib.fa_host_pipeline_destroy(None) == _lib.FA_OK
