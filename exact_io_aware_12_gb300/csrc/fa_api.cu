@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "../../include/fa.h"
 #include "fa_internal.h"
@@ -189,8 +190,55 @@ __global__ void watchdog_selftest_kernel(unsigned int* err, unsigned long long l
 
 }  // namespace
 
+namespace {
+// Encoded maps, keyed by every argument of the encode: a map only describes an
+// address, a shape and a box, so a hit is the same 128 bytes the driver would
+// produce again.  Bounded: cleared when full.
+struct MapKey {
+    uintptr_t base;
+    int dtype, esize, cols, rows, planes, box_cols, box_rows;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && dtype == o.dtype && esize == o.esize && cols == o.cols &&
+               rows == o.rows && planes == o.planes && box_cols == o.box_cols && box_rows == o.box_rows;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey& k) const {
+        uint64_t h = k.base * 0x9E3779B97F4A7C15ull;
+        const int f[] = {k.dtype, k.esize, k.cols, k.rows, k.planes, k.box_cols, k.box_rows};
+        for (int x : f) h = (h ^ static_cast<uint64_t>(x)) * 0x100000001B3ull;
+        return static_cast<size_t>(h);
+    }
+};
+constexpr size_t kMapCacheMax = 4096;
+std::mutex g_map_mutex;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash>& map_cache() {
+    static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
+    return cache;
+}
+}  // namespace
+
 bool make_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int esize,
                    int cols, int rows, int planes, int box_cols, int box_rows) {
+    const MapKey key{reinterpret_cast<uintptr_t>(base), static_cast<int>(dtype), esize, cols, rows,
+                     planes, box_cols, box_rows};
+    {
+        std::lock_guard<std::mutex> lock(g_map_mutex);
+        auto it = map_cache().find(key);
+        if (it != map_cache().end()) {
+            *map = it->second;
+            return true;
+        }
+    }
+    if (!encode_tile_map(map, base, dtype, esize, cols, rows, planes, box_cols, box_rows)) return false;
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    if (map_cache().size() >= kMapCacheMax) map_cache().clear();
+    map_cache().emplace(key, *map);
+    return true;
+}
+
+bool encode_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int esize,
+                     int cols, int rows, int planes, int box_cols, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),

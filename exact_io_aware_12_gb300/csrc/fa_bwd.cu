@@ -301,6 +301,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    griddep_launch_dependents();  // the dQ conversion kernel may be scheduled
     const uint32_t tmem = sh.tmem_base;
     const Watchdog wd{p.err, &sh.abort_flag, p.wait_limit_ns};
     constexpr uint32_t FULL = 0xffffffffu;
@@ -321,6 +322,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 tma_load_3d(sbase + L::kV + b * L::kBox, &tmV, bar_kv, b * 64, kv_start, bh);
             }
         }
+        // LSE comes from the forward and D from the D kernel launched just before
+        // this one, which may still be running (dependent launch): wait for it
+        griddep_wait();
         int qsp = -1;  // block mask: the query tile of the last step
         for (int s = 0; s < n_steps; ++s) {
             const int st = s & 1;
@@ -452,6 +456,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         // reduce-add) and, once the reads are done, hands the stage back to the
         // producer; waiting here keeps that wait off the softmax warps' path.
         if (lane == 0) {
+            griddep_wait();  // the accumulator is zeroed by the D kernel
             bool ok = true;
             int qsp = -1;  // block mask: the query tile of the last step
             for (int s = 0; s < n_steps; ++s) {
@@ -740,6 +745,9 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __
                                                          const __nv_bfloat16* __restrict__ dO,
                                                          float* __restrict__ Dvec,
                                                          float* __restrict__ dQacc, int64_t rows) {
+    // launched as a dependent of the previous kernel on the stream (usually the
+    // forward, which writes O): wait for it
+    griddep_wait();
     constexpr int TPR = D / 8;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t row = tid / TPR;
@@ -761,12 +769,17 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (row < rows && sub == 0) Dvec[row] = acc;
+    // the main kernel may be scheduled once every CTA of this one is here: its
+    // set-up and K, V loads overlap this kernel's last CTAs (it waits for this
+    // kernel to finish before reading D or reducing into the accumulator)
+    griddep_launch_dependents();
 }
 
 // dQ = bf16(tau * acc), 8 elements per thread, grid-stride.
 __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restrict__ acc,
                                                           __nv_bfloat16* __restrict__ dQ,
                                                           float tau, int64_t n8) {
+    griddep_wait();  // the accumulator is complete once the main kernel is
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
@@ -805,10 +818,9 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         constexpr int TPR = D / 8;
         const int64_t threads = rows * TPR;
         const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
-        fa_bwd_pre_kernel<D><<<blocks, 256, 0, stream>>>(
-            static_cast<const __nv_bfloat16*>(a.O), static_cast<const __nv_bfloat16*>(a.dO), a.D,
-            a.dQacc, rows);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_dependent(fa_bwd_pre_kernel<D>, dim3(blocks), dim3(256), 0, stream,
+                                         static_cast<const __nv_bfloat16*>(a.O),
+                                         static_cast<const __nv_bfloat16*>(a.dO), a.D, a.dQacc, rows);
         if (e != cudaSuccess) return e;
     }
     // 2. main kernel
@@ -826,8 +838,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         // d = 128: four elementwise warpgroups (32 query columns each); d = 64: two
         // (four measured 4-8% slower there)
         constexpr int NWG = D == 128 ? 4 : 2;
-        auto kern = fa_bwd_main_kernel<D, CAUSAL, MASK, NWG>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+        constexpr auto kern = &fa_bwd_main_kernel<D, CAUSAL, MASK, NWG>;
+        cudaError_t e = set_max_dyn_smem_once<kern>(L::kBytes);
         if (e != cudaSuccess) return e;
         BwdParams p;
         p.LSE = a.LSE;
@@ -844,8 +856,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         p.wait_limit_ns = a.wait_limit_ns;
         dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(p.n_kv));
         if (a.ev_start) cudaEventRecord(a.ev_start, stream);
-        kern<<<grid, bwd_threads(NWG), L::kBytes, stream>>>(tq, tk, tv, tdo, tacc, tdk, tdv, p);
-        e = cudaGetLastError();
+        e = launch_dependent(kern, grid, dim3(bwd_threads(NWG)), L::kBytes, stream, tq, tk, tv, tdo,
+                             tacc, tdk, tdv, p);
         if (e == cudaSuccess && a.ev_stop) e = cudaEventRecord(a.ev_stop, stream);
         if (e != cudaSuccess) return e;
     }
@@ -854,9 +866,9 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         const int64_t n8 = rows * D / 8;
         int64_t blocks = (n8 + 255) / 256;
         if (blocks > 152 * 64) blocks = 152 * 64;
-        fa_bwd_post_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            a.dQacc, static_cast<__nv_bfloat16*>(a.dQ), a.tau, n8);
-        return cudaGetLastError();
+        return launch_dependent(fa_bwd_post_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                                stream, static_cast<const float*>(a.dQacc),
+                                static_cast<__nv_bfloat16*>(a.dQ), a.tau, n8);
     }
 }
 

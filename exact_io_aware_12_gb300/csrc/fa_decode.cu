@@ -318,8 +318,8 @@ __global__ void __launch_bounds__(256) fa_decode_combine_kernel(const float* __r
 template <int D, int NQ>
 cudaError_t launch_decode_t(const DecArgs& a, cudaStream_t stream) {
     using L = DecLayout<D, NQ>;
-    auto kern = fa_decode_split_kernel<D, NQ>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    constexpr auto kern = &fa_decode_split_kernel<D, NQ>;
+    cudaError_t e = set_max_dyn_smem_once<kern>(L::kBytes);
     if (e != cudaSuccess) return e;
     DecParams p;
     p.Q = static_cast<const __nv_bfloat16*>(a.Q);

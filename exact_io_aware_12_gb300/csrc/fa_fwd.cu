@@ -241,6 +241,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // a kernel launched after this one as its programmatic dependent (the
+    // backward's D kernel) may be scheduled; it waits for this grid to finish
+    griddep_launch_dependents();
     const uint32_t tmem = sh.tmem_base;
     const Watchdog wd{p.err, &sh.abort_flag, p.wait_limit_ns};
     if constexpr (SPARSE) {
@@ -776,8 +779,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     } else if (!make_tile_map(&to, a.O, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.BH, 64, kBM)) {
         return cudaErrorInvalidValue;
     }
-    auto kern = fa_fwd_kernel<D, CAUSAL, O32, MASK, TILES>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynSmem);
+    constexpr auto kern = &fa_fwd_kernel<D, CAUSAL, O32, MASK, TILES>;
+    cudaError_t e = set_max_dyn_smem_once<kern>(L::kDynSmem);
     if (e != cudaSuccess) return e;
     FwdParams p;
     p.LSE = a.LSE;

@@ -406,8 +406,8 @@ cudaError_t launch_fp8_t(const Fp8Args& a, cudaStream_t stream) {
         !make_tile_map(&tv, a.V, U8, 1, kD, a.N, a.BH, kD, kBN) ||
         !make_tile_map(&to, a.O, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kD, a.N, a.BH, 64, kBM))
         return cudaErrorInvalidValue;
-    auto kern = fa_fwd_fp8_kernel<CAUSAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+    constexpr auto kern = &fa_fwd_fp8_kernel<CAUSAL>;
+    cudaError_t e = set_max_dyn_smem_once<kern>(kDynSmem);
     if (e != cudaSuccess) return e;
     Fp8Params p;
     p.LSE = a.LSE;

@@ -1,8 +1,10 @@
 // Host-side declarations shared by the library's translation units.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -99,9 +101,45 @@ void decode_plan(int BH, int Nk, int* splits, int* chunk);
 
 // Encodes a 3-D tiled tensor map over a contiguous [BH][N][cols] tensor with
 // a {box_cols, box_rows, 1} box and the 128-byte swizzle (box_cols * esize
-// must be 128).  Returns false if the driver rejects it.
+// must be 128).  Returns false if the driver rejects it.  make_tile_map keeps
+// the maps it has encoded and returns a kept one for the same arguments.
 bool make_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int esize,
                    int cols, int rows, int planes, int box_cols, int box_rows);
+bool encode_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int esize,
+                     int cols, int rows, int planes, int box_cols, int box_rows);
+
+// Raises a kernel's dynamic shared-memory limit to `bytes`, once per device
+// (the attribute stays set; later calls only check a flag).
+template <auto Kern>
+cudaError_t set_max_dyn_smem_once(int bytes) {
+    static std::atomic<int> done[64] = {};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+    const bool cacheable = dev >= 0 && dev < 64;
+    if (cacheable && done[dev].load(std::memory_order_acquire) == bytes) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && cacheable) done[dev].store(bytes, std::memory_order_release);
+    return e;
+}
+
+// Launches `kern` as a programmatic dependent of the previous kernel on the
+// stream: it may be scheduled before that kernel has finished, and must call
+// griddepcontrol.wait before touching anything that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);

@@ -60,6 +60,17 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t count, bool p
     return r != 0;
 }
 
+// ------------------------------------------------ dependent launches -----
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed and their memory is visible (returns at once when the grid was
+// launched without the programmatic-serialization attribute).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets a dependent grid be scheduled once every CTA of this grid has issued
+// this or exited (it still waits in griddep_wait for this grid's completion).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- mbarrier -----
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
