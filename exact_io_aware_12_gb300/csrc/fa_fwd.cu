@@ -605,8 +605,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 alpha = ex2(m_used - m_cand);  // 0 on the first block (m_used = -inf)
                 m_used = m_cand;
             }
-            l *= alpha;
-            l_mma *= alpha;
+            // unmasked kernels round the row sums' rescale and update separately (no
+            // FMA contraction), so they and the persistent short forward give the
+            // same LSE bits
+            if constexpr (MASK == kMaskNone) {
+                l = __fmul_rn(l, alpha);
+                l_mma = __fmul_rn(l_mma, alpha);
+            } else {
+                l *= alpha;
+                l_mma *= alpha;
+            }
             const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
             // Two row sums: l_mma over the bf16 P values the P.V MMA consumes (it
             // normalises O, so the weights actually applied sum to one) and l over
@@ -654,8 +662,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 lr0 = b2.x;
                 lr1 = b2.y;
             }
-            l += ls0 + ls1;
-            l_mma += lr0 + lr1;
+            if constexpr (MASK == kMaskNone) {
+                l = __fadd_rn(l, __fadd_rn(ls0, ls1));
+                l_mma = __fadd_rn(l_mma, __fadd_rn(lr0, lr1));
+            } else {
+                l += ls0 + ls1;
+                l_mma += lr0 + lr1;
+            }
             if (jj > 0 && __any_sync(0xffffffffu, grow)) {
                 // rescale this warp's 32 rows of O once P_{j-1} V_{j-1} has landed (done after
                 // P_j is written so the S registers are dead; P_j V_j waits for p_ready)
@@ -816,9 +829,7 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
         return a.d == 64 ? launch_fwd_t<64, true, false, kMaskWindow>(a, stream)
                          : launch_fwd_t<128, true, false, kMaskWindow>(a, stream);
     if (a.d == 64) {
-        if (!a.o32 && a.N <= kSingleTileMaxN)
-            return a.causal ? launch_fwd_t<64, true, false, kMaskNone, 1>(a, stream)
-                            : launch_fwd_t<64, false, false, kMaskNone, 1>(a, stream);
+        if (!a.o32 && a.N <= kSingleTileMaxN) return launch_fwd_short(a, stream);
         if (a.causal) return a.o32 ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, true, false>(a, stream);
         return a.o32 ? launch_fwd_t<64, false, true>(a, stream) : launch_fwd_t<64, false, false>(a, stream);
     }
