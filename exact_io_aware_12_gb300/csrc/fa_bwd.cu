@@ -28,6 +28,10 @@
 //             into the accumulator with TMA bulk reductions (no per-element
 //             atomics); at the end they write dK (scaled by tau) and dV.  The
 //             loader warp issues the TMA copies, the MMA warp the MMAs.
+//             Short d = 64 problems without a mask run it persistently: one CTA
+//             per SM walks a list of (key tile, batch*head) items, with the next
+//             item's K/V in a second buffer and its first S^T / dP^T issued while
+//             the elementwise warps write the current item's dK and dV.
 //   bwd_post  dQ = bf16(tau * accumulator).
 // Tensor memory (512 columns): dV and dK accumulators (d each), S^T (128),
 // dP^T (128).  P^T (bf16, two per column) is written over the first half of
@@ -38,6 +42,7 @@
 // been read out.  For d = 64, dQ has 64 columns of its own.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 #include <type_traits>
 
@@ -56,6 +61,7 @@ constexpr float kLog2e = 1.44269504088896341f;
 // Which query tiles a key tile visits beyond causality.
 enum : int { kMaskNone = 0, kMaskWindow = 1, kMaskBlocks = 2 };
 constexpr int kMaskWords = kMaxMaskBlocks / 32;
+constexpr int kBwdPersistMaxN = 2048;  // d = 64, no mask, up to this length: the persistent kernel
 
 template <int D>
 struct BwdLayout {
@@ -80,10 +86,16 @@ struct BwdLayout {
     // more than it saves
     static constexpr bool kDSInTmem = (D == 128);
     static constexpr uint32_t kTmDQ = kDQAliasDP ? kTmDP : 2 * D + 256;
+    // persistent kernel: a second K/V buffer (K at +0, V at +kTile), so the next
+    // work item's tiles load during this one, and a dV/dK staging area of its own
+    static constexpr int kKV1 = (kBytes + 1023) / 1024 * 1024;
+    static constexpr int kStageKV = kKV1 + 2 * kTile;
+    static constexpr int kBytesPersist = kStageKV + 2 * kTile;
 };
 
 struct BwdBarriers {
-    uint64_t kv_full;
+    uint64_t kv_full[2];   // K/V buffer b loaded (one buffer unless persistent)
+    uint64_t kv_empty[2];  // persistent: the MMAs of the item in K/V buffer b are done
     uint64_t q_full[2];    // Q tile (and the LSE / D vectors) of stage s loaded
     uint64_t do_full[2];   // dO tile of stage s loaded
     uint64_t q_empty[2];   // stage s's Q half free: MMAs done, staged dQ half read
@@ -115,6 +127,8 @@ struct BwdParams {
     const uint8_t* blocks;          // block mask [heads][n_kv][n_kv] (kMaskBlocks)
     long long blocks_head_stride;   // bytes between heads' masks (0: one mask)
     int head_group;                 // heads whose key tiles are interleaved in launch order
+    int BH;                         // persistent: batch*heads
+    int items;                      // persistent: work items (BH key tiles each)
 };
 
 enum : uint32_t {
@@ -182,8 +196,9 @@ __device__ __forceinline__ void mma_mn_mn(uint32_t tmem_d, uint32_t a_lo, uint32
 }
 
 // MASK: kMaskNone; kMaskWindow, a causal sliding window of p.window keys (only
-// with CAUSAL); kMaskBlocks, the block mask p.blocks.
-template <int D, bool CAUSAL, int MASK, int NWG>
+// with CAUSAL); kMaskBlocks, the block mask p.blocks.  PERSIST: one CTA per SM
+// walks a list of (key tile, batch*head) work items (no mask).
+template <int D, bool CAUSAL, int MASK, int NWG, bool PERSIST = false>
 __global__ void __launch_bounds__(bwd_threads(NWG), 1)
 fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -194,6 +209,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     static_assert(sizeof(BwdBarriers) <= L::kBytes - L::kBars, "barrier block overflows its slot");
     static_assert(NWG == 2 || NWG == 4, "two or four elementwise warpgroups");
     static_assert((D / NWG) % 16 == 0, "each warpgroup drains whole 16-column chunks");
+    static_assert(!PERSIST || MASK == kMaskNone, "the persistent kernel takes no mask");
     constexpr int kProducerWarp = 4 * NWG, kMmaWarp = 4 * NWG + 1, kReducerWarp = 4 * NWG + 2;
     constexpr int kQC = 128 / NWG;      // query columns of P^T / dS^T per warpgroup
     constexpr int kDC = D / NWG;        // d-columns of dQ, dK, dV per warpgroup
@@ -208,20 +224,37 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Launch order (x fastest) walks groups of p.head_group heads; inside a group
-    // the key tiles go in order (tile 0 has the most query tiles when causal),
-    // the group's heads interleaved.  So the CTAs resident at one time work on
-    // a few heads, whose Q, dO and fp32 dQ accumulator stay in L2.
-    int bh, kv_tile;
-    {
+    // Work item k of this CTA: (batch*head, key tile), or false past the last.
+    // Without PERSIST a CTA has one item, set by its launch position: the launch
+    // order (x fastest) walks groups of p.head_group heads; inside a group the key
+    // tiles go in order (tile 0 has the most query tiles when causal), the group's
+    // heads interleaved.  So the CTAs resident at one time work on a few heads,
+    // whose Q, dO and fp32 dQ accumulator stay in L2.  With PERSIST, CTA c of G
+    // takes items c, 2G - 1 - c, 2G + c, ... of the list ordered by key tile, then
+    // head (heaviest first when causal): a snake that balances heavy and light
+    // items without a shared counter.  (The head-grouped order measured slower
+    // here: at these sizes the balance matters more than the L2 reuse.)
+    auto item_at = [&](int k, int& ibh, int& ikv) -> bool {
+        if constexpr (PERSIST) {
+            const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+            const long long i = static_cast<long long>(k) * G + ((k & 1) ? G - 1 - c : c);
+            if (i >= p.items) return false;
+            ikv = static_cast<int>(i / p.BH);
+            ibh = static_cast<int>(i - static_cast<long long>(ikv) * p.BH);
+            return true;
+        }
+        if (k > 0) return false;
         const long long i = blockIdx.x + static_cast<long long>(gridDim.x) * blockIdx.y;
-        const long long per_group = static_cast<long long>(p.head_group) * gridDim.y;
+        const long long per_group = static_cast<long long>(p.head_group) * p.n_kv;
         const int g = static_cast<int>(i / per_group);
         const int j = static_cast<int>(i - g * per_group);
-        const int heads = min(p.head_group, static_cast<int>(gridDim.x) - g * p.head_group);
-        kv_tile = j / heads;
-        bh = g * p.head_group + (j - kv_tile * heads);
-    }
+        const int heads = min(p.head_group, p.BH - g * p.head_group);
+        ikv = j / heads;
+        ibh = g * p.head_group + (j - ikv * heads);
+        return true;
+    };
+    int bh = 0, kv_tile = 0;  // item 0 (every CTA has one)
+    item_at(0, bh, kv_tile);
     const int N = p.N;
     const int kv_start = kv_tile * kBK;
     const int n_q = (N + kBQ - 1) / kBQ;
@@ -231,13 +264,17 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const int first = CAUSAL ? kv_tile : 0;
     const int last = window > 0 ? min(n_q - 1, (kv_start + kBK - 1 + window - 1) / kBQ) : n_q - 1;
     int n_steps = last - first + 1;  // with a block mask: counted below
+    // an item's first query tile and step count (item 0: first and n_steps)
+    auto first_of = [&](int ikv) { return PERSIST ? (CAUSAL ? ikv : 0) : first; };
+    auto steps_of = [&](int ikv) { return PERSIST ? n_q - (CAUSAL ? ikv : 0) : n_steps; };
 
     if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
         if (threadIdx.x == 0) atomicCAS(p.err, 0u, 1u | (0xAAu << 8));
         return;
     }
 
-    const uint32_t bar_kv = smem_addr(&sh.kv_full);
+    const uint32_t bar_kv = smem_addr(&sh.kv_full[0]);
+    const uint32_t bar_kve = smem_addr(&sh.kv_empty[0]);
     const uint32_t bar_qf = smem_addr(&sh.q_full[0]);
     const uint32_t bar_df = smem_addr(&sh.do_full[0]);
     const uint32_t bar_qe = smem_addr(&sh.q_empty[0]);
@@ -254,7 +291,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
     if (threadIdx.x == 0) {
         sh.abort_flag = 0;
-        mbar_init(bar_kv, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_kv + 8 * b, 1);
+            mbar_init(bar_kve + 8 * b, 1);
+        }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar_qf + 8 * s, 32);
             mbar_init(bar_df + 8 * s, 1);
@@ -313,70 +353,93 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------- producer --
-        // a key tile that no query tile visits (block mask) loads nothing: its
-        // epilogue writes zero dK, dV over the K and V tiles
-        if (lane == 0 && (!SPARSE || n_steps > 0)) {
-            mbar_arrive_expect_tx(bar_kv, 2 * L::kTile);
-            for (int b = 0; b < L::kBoxes; ++b) {
-                tma_load_3d(sbase + L::kK + b * L::kBox, &tmK, bar_kv, b * 64, kv_start, bh);
-                tma_load_3d(sbase + L::kV + b * L::kBox, &tmV, bar_kv, b * 64, kv_start, bh);
+        // Steps are numbered across work items (gs): the Q/dO stage and the
+        // barrier phases follow gs, the K/V buffer follows the item.
+        bool pok = true;
+        int gs = 0;
+        int ibh = 0, ikv = 0;
+        for (int k = 0; pok && item_at(k, ibh, ikv); ++k) {
+            const int kb = PERSIST ? (k & 1) : 0;
+            const int ifirst = first_of(ikv), isteps = steps_of(ikv);
+            // the buffer's previous item (k - 2) must be done with it
+            if (PERSIST && k >= 2 && !mbar_wait(bar_kve + 8 * kb, ((k >> 1) - 1) & 1, wd, kSiteProd)) break;
+            // a key tile that no query tile visits (block mask) loads nothing: its
+            // epilogue writes zero dK, dV over the K and V tiles
+            if (lane == 0 && (!SPARSE || isteps > 0)) {
+                const uint32_t kv_buf = sbase + (kb ? L::kKV1 : L::kK);
+                mbar_arrive_expect_tx(bar_kv + 8 * kb, 2 * L::kTile);
+                for (int b = 0; b < L::kBoxes; ++b) {
+                    tma_load_3d(kv_buf + b * L::kBox, &tmK, bar_kv + 8 * kb, b * 64, ikv * kBK, ibh);
+                    tma_load_3d(kv_buf + L::kTile + b * L::kBox, &tmV, bar_kv + 8 * kb, b * 64, ikv * kBK,
+                                ibh);
+                }
             }
-        }
-        // LSE comes from the forward and D from the D kernel launched just before
-        // this one, which may still be running (dependent launch): wait for it
-        griddep_wait();
-        int qsp = -1;  // block mask: the query tile of the last step
-        for (int s = 0; s < n_steps; ++s) {
-            const int st = s & 1;
-            int qtile = first + s;
-            if constexpr (SPARSE) {
-                qsp = next_set_bit(sh.qbits, nullptr, qsp + 1, n_q);
-                qtile = qsp;
-            }
-            const int q_start = qtile * kBQ;
-            const int64_t row0 = static_cast<int64_t>(bh) * N;
-            // this step's LSE and D into registers first: their latency overlaps
-            // the wait for the stage (stored negated: the softmax warps add them
-            // with paired fp32 ops)
-            float lv[4], dv[4];
+            // LSE comes from the forward and D from the D kernel launched just before
+            // this one, which may still be running (dependent launch): wait for it
+            if (k == 0) griddep_wait();
+            int qsp = -1;  // block mask: the query tile of the last step
+            for (int s = 0; s < isteps; ++s, ++gs) {
+                if constexpr (!PERSIST) gs = s;  // one item: the two counts agree
+                const int st = gs & 1;
+                int qtile = ifirst + s;
+                if constexpr (SPARSE) {
+                    qsp = next_set_bit(sh.qbits, nullptr, qsp + 1, n_q);
+                    qtile = qsp;
+                }
+                const int q_start = qtile * kBQ;
+                const int64_t row0 = static_cast<int64_t>(ibh) * N;
+                // this step's LSE and D into registers first: their latency overlaps
+                // the wait for the stage (stored negated: the softmax warps add them
+                // with paired fp32 ops)
+                float lv[4], dv[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int q = q_start + lane * 4 + e;
-                lv[e] = q < N ? -p.LSE[row0 + q] * kLog2e : -INFINITY;
-                dv[e] = q < N ? -p.Dvec[row0 + q] : 0.f;
-            }
-            // the two halves of the stage are refilled as each is freed: dO (whose
-            // staged dQ half is added first), then Q with the vectors
-            const uint32_t stage = sbase + L::kStage0 + st * L::kStageBytes;
-            if (s >= 2 && !mbar_wait(bar_de + 8 * st, ((s >> 1) - 1) & 1, wd, kSiteProd)) break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar_df + 8 * st, L::kTile);
-                for (int b = 0; b < L::kBoxes; ++b)
-                    tma_load_3d(stage + L::kTile + b * L::kBox, &tmdO, bar_df + 8 * st, b * 64,
-                                q_start, bh);
-            }
-            if (s >= 2 && !mbar_wait(bar_qe + 8 * st, ((s >> 1) - 1) & 1, wd, kSiteProd)) break;
-            if (lane == 0) {  // the bulk copy first, then the vectors
-                mbar_expect_tx(bar_qf + 8 * st, L::kTile);
-                for (int b = 0; b < L::kBoxes; ++b)
-                    tma_load_3d(stage + b * L::kBox, &tmQ, bar_qf + 8 * st, b * 64, q_start, bh);
-            }
+                for (int e = 0; e < 4; ++e) {
+                    const int q = q_start + lane * 4 + e;
+                    lv[e] = q < N ? -p.LSE[row0 + q] * kLog2e : -INFINITY;
+                    dv[e] = q < N ? -p.Dvec[row0 + q] : 0.f;
+                }
+                // the two halves of the stage are refilled as each is freed: dO (whose
+                // staged dQ half is added first), then Q with the vectors
+                const uint32_t stage = sbase + L::kStage0 + st * L::kStageBytes;
+                if (gs >= 2 && !mbar_wait(bar_de + 8 * st, ((gs >> 1) - 1) & 1, wd, kSiteProd)) {
+                    pok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar_df + 8 * st, L::kTile);
+                    for (int b = 0; b < L::kBoxes; ++b)
+                        tma_load_3d(stage + L::kTile + b * L::kBox, &tmdO, bar_df + 8 * st, b * 64,
+                                    q_start, ibh);
+                }
+                if (gs >= 2 && !mbar_wait(bar_qe + 8 * st, ((gs >> 1) - 1) & 1, wd, kSiteProd)) {
+                    pok = false;
+                    break;
+                }
+                if (lane == 0) {  // the bulk copy first, then the vectors
+                    mbar_expect_tx(bar_qf + 8 * st, L::kTile);
+                    for (int b = 0; b < L::kBoxes; ++b)
+                        tma_load_3d(stage + b * L::kBox, &tmQ, bar_qf + 8 * st, b * 64, q_start, ibh);
+                }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                lse2_s[st * 128 + lane * 4 + e] = lv[e];
-                dvec_s[st * 128 + lane * 4 + e] = dv[e];
+                for (int e = 0; e < 4; ++e) {
+                    lse2_s[st * 128 + lane * 4 + e] = lv[e];
+                    dvec_s[st * 128 + lane * 4 + e] = dv[e];
+                }
+                mbar_arrive(bar_qf + 8 * st);  // 32 arrivals; the phase also waits for the copy
             }
-            mbar_arrive(bar_qf + 8 * st);  // 32 arrivals; the phase also waits for the copy
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA --
         // The whole warp runs this loop; each MMA and commit is issued by one
         // elected lane (see mma_ss_warp).
         {
-            // low descriptor halves: K-major (LBO unused) and MN-major (LBO = 16 KB)
-            const uint32_t k_lo = sw128_desc_lo(sbase + L::kK, 16);
-            const uint32_t k_mn = sw128_desc_lo(sbase + L::kK, kLboMN);
-            const uint32_t v_lo = sw128_desc_lo(sbase + L::kV, 16);
+            // low descriptor halves: K-major (LBO unused) and MN-major (LBO = 16 KB);
+            // K and V per buffer (buffer 1 only in the persistent kernel)
+            const uint32_t k_lo0 = sw128_desc_lo(sbase + L::kK, 16), k_lo1 = sw128_desc_lo(sbase + L::kKV1, 16);
+            const uint32_t k_mn0 = sw128_desc_lo(sbase + L::kK, kLboMN);
+            const uint32_t k_mn1 = sw128_desc_lo(sbase + L::kKV1, kLboMN);
+            const uint32_t v_lo0 = sw128_desc_lo(sbase + L::kV, 16);
+            const uint32_t v_lo1 = sw128_desc_lo(sbase + L::kKV1 + L::kTile, 16);
             const uint32_t ds_mn = sw128_desc_lo(sbase + L::kDS, kLboMN);
             const uint32_t ds_lo = sw128_desc_lo(sbase + L::kDS, 16);
             const uint32_t q_lo0 = sw128_desc_lo(sbase + L::kStage0, 16);
@@ -389,63 +452,84 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                                                   mbar_wait(bar_qf, 0, wd, kSiteMmaQ));
             if (ok) {
                 tc_fence_after();
-                mma_rows_rows<D>(tmem + L::kTmS, k_lo, q_lo0);     // S^T
+                mma_rows_rows<D>(tmem + L::kTmS, k_lo0, q_lo0);     // S^T
                 mma_commit_warp(bar_s);
                 ok = __all_sync(0xffffffffu, mbar_wait(bar_df, 0, wd, kSiteMmaQ));
                 if (ok) {
                     tc_fence_after();
-                    mma_rows_rows<D>(tmem + L::kTmDP, v_lo, do_lo0);   // dP^T
+                    mma_rows_rows<D>(tmem + L::kTmDP, v_lo0, do_lo0);   // dP^T
                     mma_commit_warp(bar_dp);
                 }
             }
-            for (int s = 0; ok && s < n_steps; ++s) {
-                const int st = s & 1;
-                const uint32_t so = st * kStageStep;
-                if (!__all_sync(0xffffffffu, mbar_wait(bar_p, s & 1, wd, kSiteMmaP))) { ok = false; break; }
-                tc_fence_after();
-                mma_tmem_a<D, kQC>(tmem + L::kTmDV, tmem + L::kTmS, do_mn0 + so, s > 0);   // dV
-                mma_commit_warp(bar_de + 8 * st);  // the last MMA that reads this dO
-                if (!__all_sync(0xffffffffu, mbar_wait(bar_ds, s & 1, wd, kSiteMmaDS))) { ok = false; break; }
-                tc_fence_after();
-                // d = 64: the dQ columns are reused every step
-                if (!L::kDQAliasDP && s > 0) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(bar_dr, (s - 1) & 1, wd, kSiteMmaDrain))) { ok = false; break; }
+            int gs = 0;  // steps across work items
+            int ibh = 0, ikv = 0;
+            for (int k = 0; ok && item_at(k, ibh, ikv); ++k) {
+                const int kb = PERSIST ? (k & 1) : 0;
+                const int isteps = steps_of(ikv);
+                int nbh = 0, nkv = 0;
+                const bool has_next = PERSIST && item_at(k + 1, nbh, nkv);
+                for (int s = 0; ok && s < isteps; ++s, ++gs) {
+                    if constexpr (!PERSIST) gs = s;  // one item: the two counts agree
+                    const int st = gs & 1;
+                    const uint32_t so = st * kStageStep;
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_p, gs & 1, wd, kSiteMmaP))) { ok = false; break; }
                     tc_fence_after();
-                }
-                // dQ first: its drain is on the elementwise warps' path; dK and the
-                // next S^T run while they drain it
-                mma_mn_mn<D>(tmem + L::kTmDQ, ds_mn, k_mn);                            // dQ
-                mma_commit_warp(bar_dq);
-                if constexpr (L::kDSInTmem)
-                    mma_tmem_a<D, kQC>(tmem + L::kTmDK, tmem + L::kTmS + kQC / 2, q_mn0 + so, s > 0);  // dK
-                else
-                    mma_rows_mn<D>(tmem + L::kTmDK, ds_lo, q_mn0 + so, s > 0);           // dK
-                mma_commit_warp(bar_dk);           // d = 64: also, the dS^T tile is free again
-                mma_commit_warp(bar_qe + 8 * st);
-                if (s + 1 < n_steps) {
-                    const int st1 = (s + 1) & 1;
-                    const uint32_t so1 = st1 * kStageStep;
-                    if (!__all_sync(0xffffffffu, mbar_wait(bar_qf + 8 * st1, ((s + 1) >> 1) & 1, wd, kSiteMmaQ))) {
-                        ok = false;
-                        break;
-                    }
+                    mma_tmem_a<D, kQC>(tmem + L::kTmDV, tmem + L::kTmS, do_mn0 + so, s > 0);   // dV
+                    mma_commit_warp(bar_de + 8 * st);  // the last MMA that reads this dO
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_ds, gs & 1, wd, kSiteMmaDS))) { ok = false; break; }
                     tc_fence_after();
-                    // S^T over P^T and dS^T, which only the dV and dK MMAs above
-                    // read (the tensor pipe runs in issue order)
-                    mma_rows_rows<D>(tmem + L::kTmS, k_lo, q_lo0 + so1);     // S^T next
-                    mma_commit_warp(bar_s);
-                    // d = 128: dP^T over the dQ tile, once it has been read out
-                    if (L::kDQAliasDP) {
-                        if (!__all_sync(0xffffffffu, mbar_wait(bar_dr, s & 1, wd, kSiteMmaDrain))) { ok = false; break; }
+                    // d = 64: the dQ columns are reused every step
+                    if (!L::kDQAliasDP && gs > 0) {
+                        if (!__all_sync(0xffffffffu, mbar_wait(bar_dr, (gs - 1) & 1, wd, kSiteMmaDrain))) { ok = false; break; }
                         tc_fence_after();
                     }
-                    if (!__all_sync(0xffffffffu, mbar_wait(bar_df + 8 * st1, ((s + 1) >> 1) & 1, wd, kSiteMmaQ))) {
-                        ok = false;
-                        break;
+                    // dQ first: its drain is on the elementwise warps' path; dK and the
+                    // next S^T run while they drain it
+                    mma_mn_mn<D>(tmem + L::kTmDQ, ds_mn, kb ? k_mn1 : k_mn0);                        // dQ
+                    mma_commit_warp(bar_dq);
+                    if constexpr (L::kDSInTmem)
+                        mma_tmem_a<D, kQC>(tmem + L::kTmDK, tmem + L::kTmS + kQC / 2, q_mn0 + so, s > 0);  // dK
+                    else
+                        mma_rows_mn<D>(tmem + L::kTmDK, ds_lo, q_mn0 + so, s > 0);           // dK
+                    mma_commit_warp(bar_dk);           // d = 64: also, the dS^T tile is free again
+                    mma_commit_warp(bar_qe + 8 * st);
+                    const bool last_step = s + 1 == isteps;
+                    // the last MMA that reads this item's K and V has been issued
+                    if (PERSIST && last_step) mma_commit_warp(bar_kve + 8 * kb);
+                    if (!last_step || has_next) {
+                        // the next step: this item's, or the next item's first (its K, V
+                        // in the other buffer)
+                        const int nkb = last_step ? (k + 1) & 1 : kb;
+                        if (last_step) {
+                            if (!__all_sync(0xffffffffu, mbar_wait(bar_kv + 8 * nkb, ((k + 1) >> 1) & 1, wd, kSiteMmaKV))) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        const int st1 = (gs + 1) & 1;
+                        const uint32_t so1 = st1 * kStageStep;
+                        if (!__all_sync(0xffffffffu, mbar_wait(bar_qf + 8 * st1, ((gs + 1) >> 1) & 1, wd, kSiteMmaQ))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        // S^T over P^T and dS^T, which only the dV and dK MMAs above
+                        // read (the tensor pipe runs in issue order)
+                        mma_rows_rows<D>(tmem + L::kTmS, nkb ? k_lo1 : k_lo0, q_lo0 + so1);     // S^T next
+                        mma_commit_warp(bar_s);
+                        // d = 128: dP^T over the dQ tile, once it has been read out
+                        if (L::kDQAliasDP) {
+                            if (!__all_sync(0xffffffffu, mbar_wait(bar_dr, gs & 1, wd, kSiteMmaDrain))) { ok = false; break; }
+                            tc_fence_after();
+                        }
+                        if (!__all_sync(0xffffffffu, mbar_wait(bar_df + 8 * st1, ((gs + 1) >> 1) & 1, wd, kSiteMmaQ))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        mma_rows_rows<D>(tmem + L::kTmDP, nkb ? v_lo1 : v_lo0, do_lo0 + so1);   // dP^T next
+                        mma_commit_warp(bar_dp);
                     }
-                    tc_fence_after();
-                    mma_rows_rows<D>(tmem + L::kTmDP, v_lo, do_lo0 + so1);   // dP^T next
-                    mma_commit_warp(bar_dp);
                 }
             }
         }
@@ -458,34 +542,40 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         if (lane == 0) {
             griddep_wait();  // the accumulator is zeroed by the D kernel
             bool ok = true;
-            int qsp = -1;  // block mask: the query tile of the last step
-            for (int s = 0; s < n_steps; ++s) {
-                const int st = s & 1;
-                int qtile = first + s;
-                if constexpr (SPARSE) {
-                    qsp = next_set_bit(sh.qbits, nullptr, qsp + 1, n_q);
-                    qtile = qsp;
+            int gs = 0;  // steps across work items
+            int ibh = 0, ikv = 0;
+            for (int k = 0; item_at(k, ibh, ikv); ++k) {
+                const int ifirst = first_of(ikv), isteps = steps_of(ikv);
+                int qsp = -1;  // block mask: the query tile of the last step
+                for (int s = 0; s < isteps; ++s, ++gs) {
+                    if constexpr (!PERSIST) gs = s;  // one item: the two counts agree
+                    const int st = gs & 1;
+                    int qtile = ifirst + s;
+                    if constexpr (SPARSE) {
+                        qsp = next_set_bit(sh.qbits, nullptr, qsp + 1, n_q);
+                        qtile = qsp;
+                    }
+                    const uint32_t src = sbase + L::kStage0 + st * L::kStageBytes;
+                    const int q_start = qtile * kBQ;
+                    // dQ columns [D/2, D) were staged over dO (first), [0, D/2) over Q
+                    // (once dK is done)
+                    if (ok) ok = mbar_wait(bar_sgd, gs & 1, wd, kSiteReduce);
+                    if (ok) {
+                        for (int b = D / 64; b < D / 32; ++b)
+                            tma_reduce_add_3d(&tmdQacc, src + b * L::kBox, b * 32, q_start, ibh);
+                        bulk_commit();
+                    }
+                    if (ok) ok = mbar_wait(bar_sgq, gs & 1, wd, kSiteReduce);
+                    if (ok) {
+                        for (int b = 0; b < D / 64; ++b)
+                            tma_reduce_add_3d(&tmdQacc, src + b * L::kBox, b * 32, q_start, ibh);
+                        bulk_commit();
+                        bulk_wait_read<1>();
+                    }
+                    mbar_arrive(bar_de + 8 * st);
+                    if (ok) bulk_wait_read<0>();
+                    mbar_arrive(bar_qe + 8 * st);
                 }
-                const uint32_t src = sbase + L::kStage0 + st * L::kStageBytes;
-                const int q_start = qtile * kBQ;
-                // dQ columns [D/2, D) were staged over dO (first), [0, D/2) over Q
-                // (once dK is done)
-                if (ok) ok = mbar_wait(bar_sgd, s & 1, wd, kSiteReduce);
-                if (ok) {
-                    for (int b = D / 64; b < D / 32; ++b)
-                        tma_reduce_add_3d(&tmdQacc, src + b * L::kBox, b * 32, q_start, bh);
-                    bulk_commit();
-                }
-                if (ok) ok = mbar_wait(bar_sgq, s & 1, wd, kSiteReduce);
-                if (ok) {
-                    for (int b = 0; b < D / 64; ++b)
-                        tma_reduce_add_3d(&tmdQacc, src + b * L::kBox, b * 32, q_start, bh);
-                    bulk_commit();
-                    bulk_wait_read<1>();
-                }
-                mbar_arrive(bar_de + 8 * st);
-                if (ok) bulk_wait_read<0>();
-                mbar_arrive(bar_qe + 8 * st);
             }
         }
         __syncwarp();
@@ -497,7 +587,6 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         // thread still reaches every named barrier, so none can be left waiting.
         const int h = warp >> 2;
         const int r = threadIdx.x & 127;  // key row (P^T, dS^T, dK, dV) / query row (dQ)
-        const int kg = kv_start + r;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_off + L::kTmS + kQC * h;
         const uint32_t tDP = tmem + lane_off + L::kTmDP + kQC * h;
@@ -509,223 +598,243 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         const int ds_chunk0 = (kQC * h % 64) / 8;
         constexpr int kDrainChunks = kDC / 16;  // 16-column fp32 chunks of dQ per warpgroup
         bool ok = true;
-        int qsp = -1;  // block mask: the query tile of the last step
-        for (int s = 0; s < n_steps; ++s) {
-            const int st = s & 1;
-            int qtile = first + s;
-            if constexpr (SPARSE) {
-                qsp = next_set_bit(sh.qbits, nullptr, qsp + 1, n_q);
-                qtile = qsp;
-            }
-            const int q_start = qtile * kBQ;
-            // P^T = exp2(c S^T - log2e LSE), bf16, over this warpgroup's S^T columns.
-            // -log2(e) LSE per query, pairs of adjacent queries as one 64-bit value,
-            // read four queries per 16-byte broadcast load; the first chunk's are
-            // read as soon as the stage (with the vectors) is in, before S^T is
-            const ulonglong2* nl4 = reinterpret_cast<const ulonglong2*>(lse2_s + st * 128 + kQC * h);
-            ulonglong2 nl0[8];
-            uint32_t pkeep[16];  // the first chunk's packed P^T, reused by dS^T below
-            if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_qf + 8 * st, (s >> 1) & 1, wd, kSiteDsQ));
-            if (ok) {
+        int gs = 0;  // steps across work items
+        int ibh = 0, ikv = 0;
+        for (int k = 0; item_at(k, ibh, ikv); ++k) {
+            const int ifirst = first_of(ikv), isteps = steps_of(ikv);
+            const int kvs = ikv * kBK;
+            const int kg = kvs + r;
+            int qsp = -1;  // block mask: the query tile of the last step
+            for (int s = 0; s < isteps; ++s, ++gs) {
+                if constexpr (!PERSIST) gs = s;  // one item: the two counts agree
+                const int st = gs & 1;
+                int qtile = ifirst + s;
+                if constexpr (SPARSE) {
+                    qsp = next_set_bit(sh.qbits, nullptr, qsp + 1, n_q);
+                    qtile = qsp;
+                }
+                const int q_start = qtile * kBQ;
+                // P^T = exp2(c S^T - log2e LSE), bf16, over this warpgroup's S^T columns.
+                // -log2(e) LSE per query, pairs of adjacent queries as one 64-bit value,
+                // read four queries per 16-byte broadcast load; the first chunk's are
+                // read as soon as the stage (with the vectors) is in, before S^T is
+                const ulonglong2* nl4 = reinterpret_cast<const ulonglong2*>(lse2_s + st * 128 + kQC * h);
+                ulonglong2 nl0[8];
+                uint32_t pkeep[16];  // the first chunk's packed P^T, reused by dS^T below
+                if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_qf + 8 * st, (gs >> 1) & 1, wd, kSiteDsQ));
+                if (ok) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) nl0[i] = nl4[i];
-            }
-            if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_s, s & 1, wd, kSiteDsS));
-            if (ok) {
-                tc_fence_after();
-                const bool diag = CAUSAL && (q_start == kv_start);
-                // window edge: query q no longer sees key kg once q >= kg + window
-                const bool wedge = window > 0 && q_start + kBQ - 1 >= kv_start + window;
-                const int qh = q_start + kQC * h;
-                const uint64_t c2 = f2_pack(sl2, sl2);
-                // most tiles need no mask: the loop is built twice, and the masked
-                // copy runs only on the diagonal, window-edge and ragged-end tiles
-                const bool masked = diag || wedge || kv_start + kBK > N;
+                    for (int i = 0; i < 8; ++i) nl0[i] = nl4[i];
+                }
+                if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_s, gs & 1, wd, kSiteDsS));
+                if (ok) {
+                    tc_fence_after();
+                    const bool diag = CAUSAL && (q_start == kvs);
+                    // window edge: query q no longer sees key kg once q >= kg + window
+                    const bool wedge = window > 0 && q_start + kBQ - 1 >= kvs + window;
+                    const int qh = q_start + kQC * h;
+                    const uint64_t c2 = f2_pack(sl2, sl2);
+                    // most tiles need no mask: the loop is built twice, and the masked
+                    // copy runs only on the diagonal, window-edge and ragged-end tiles
+                    const bool masked = diag || wedge || kvs + kBK > N;
 #pragma unroll
-                for (int c = 0; c < kQC / 32; ++c) {
-                    uint32_t sv[32];
-                    tmem_ld32(tS + 32 * c, sv);
-                    tmem_ld_wait(sv);
-                    uint32_t pk[16];
-                    ulonglong2 nl[8];
+                    for (int c = 0; c < kQC / 32; ++c) {
+                        uint32_t sv[32];
+                        tmem_ld32(tS + 32 * c, sv);
+                        tmem_ld_wait(sv);
+                        uint32_t pk[16];
+                        ulonglong2 nl[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) nl[i] = c == 0 ? nl0[i] : nl4[8 * c + i];
-                    auto p_pairs = [&](auto with_mask) {
+                        for (int i = 0; i < 8; ++i) nl[i] = c == 0 ? nl0[i] : nl4[8 * c + i];
+                        auto p_pairs = [&](auto with_mask) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const int q = 32 * c + 2 * i;
+                                const uint64_t nlq = (i & 1) ? nl[i >> 1].y : nl[i >> 1].x;
+                                const float2 x = f2_unpack(
+                                    ffma2(f2_pack(u2f(sv[2 * i]), u2f(sv[2 * i + 1])), c2, nlq));
+                                float p0 = ex2(x.x);
+                                float p1 = ex2(x.y);
+                                if constexpr (decltype(with_mask)::value) {
+                                    if (diag) {
+                                        if (kg > qh + q) p0 = 0.f;
+                                        if (kg > qh + q + 1) p1 = 0.f;
+                                    }
+                                    if constexpr (LOCAL) {
+                                        if (wedge) {
+                                            if (qh + q >= kg + window) p0 = 0.f;
+                                            if (qh + q + 1 >= kg + window) p1 = 0.f;
+                                        }
+                                    }
+                                    if (kg >= N) p0 = p1 = 0.f;  // key row past a ragged end
+                                }
+                                pk[i] = pack_bf16(p0, p1);
+                            }
+                        };
+                        if (masked) p_pairs(std::true_type{});
+                        else p_pairs(std::false_type{});
+                        tmem_st16(tS + 16 * c, pk);
+                        if (c == 0) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) pkeep[i] = pk[i];
+                        }
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                }
+                mbar_arrive(bar_p);
+
+                // dS^T = P^T o (dP^T - D), to the smem tile that the dQ MMA reads (and at
+                // d = 64 the dK MMA), once the MMAs of the previous step are done with
+                // it, and at d = 128 also to tensor memory beside P^T (dK's A operand).
+                // -D per query, pairs of adjacent queries as one 64-bit value (16-byte
+                // loads); the first chunk's are read before the wait for dP^T
+                const ulonglong2* nd4 = reinterpret_cast<const ulonglong2*>(dvec_s + st * 128 + kQC * h);
+                ulonglong2 nd0[8];
+                if (ok) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) nd0[i] = nd4[i];
+                }
+                if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_dp, gs & 1, wd, kSiteDsDP) &&
+                                                  (gs == 0 || mbar_wait_sleep(L::kDSInTmem ? bar_dq : bar_dk, (gs - 1) & 1, wd,
+                                                                             kSiteDsDQ)));
+                if (ok) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < kQC / 32; ++c) {
+                        uint32_t dp[32], pk[16];
+                        tmem_ld32(tDP + 32 * c, dp);
+                        if (c == 0) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) pk[i] = pkeep[i];
+                        } else {
+                            tmem_ld16(tS + 16 * c, pk);
+                            tmem_ld_wait(pk);
+                        }
+                        tmem_ld_wait(dp);
+                        uint32_t ds[16];
+                        ulonglong2 nd[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) nd[i] = c == 0 ? nd0[i] : nd4[8 * c + i];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const int q = 32 * c + 2 * i;
-                            const uint64_t nlq = (i & 1) ? nl[i >> 1].y : nl[i >> 1].x;
-                            const float2 x = f2_unpack(
-                                ffma2(f2_pack(u2f(sv[2 * i]), u2f(sv[2 * i + 1])), c2, nlq));
-                            float p0 = ex2(x.x);
-                            float p1 = ex2(x.y);
-                            if constexpr (decltype(with_mask)::value) {
-                                if (diag) {
-                                    if (kg > qh + q) p0 = 0.f;
-                                    if (kg > qh + q + 1) p1 = 0.f;
-                                }
-                                if constexpr (LOCAL) {
-                                    if (wedge) {
-                                        if (qh + q >= kg + window) p0 = 0.f;
-                                        if (qh + q + 1 >= kg + window) p1 = 0.f;
-                                    }
-                                }
-                                if (kg >= N) p0 = p1 = 0.f;  // key row past a ragged end
-                            }
-                            pk[i] = pack_bf16(p0, p1);
+                            const uint64_t ndq = (i & 1) ? nd[i >> 1].y : nd[i >> 1].x;
+                            // dP - D in fp32, rounded to bf16, times the bf16 P
+                            const float2 t = f2_unpack(
+                                fadd2(f2_pack(u2f(dp[2 * i]), u2f(dp[2 * i + 1])), ndq));
+                            ds[i] = mul_bf16x2(pk[i], pack_bf16(t.x, t.y));
                         }
-                    };
-                    if (masked) p_pairs(std::true_type{});
-                    else p_pairs(std::false_type{});
-                    tmem_st16(tS + 16 * c, pk);
-                    if (c == 0) {
+                        if constexpr (L::kDSInTmem) tmem_st16(tS + kQC / 2 + 16 * c, ds);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) pkeep[i] = pk[i];
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const int chunk = ds_chunk0 + 4 * c + q4;
+                            *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
+                                make_uint4(ds[4 * q4], ds[4 * q4 + 1], ds[4 * q4 + 2], ds[4 * q4 + 3]);
+                        }
                     }
+                    fence_async_shared();
+                    if constexpr (L::kDSInTmem) tmem_st_wait();
+                    tc_fence_before();
                 }
-                tmem_st_wait();
-                tc_fence_before();
-            }
-            mbar_arrive(bar_p);
+                mbar_arrive(bar_ds);
 
-            // dS^T = P^T o (dP^T - D), to the smem tile that the dQ MMA reads (and at
-            // d = 64 the dK MMA), once the MMAs of the previous step are done with
-            // it, and at d = 128 also to tensor memory beside P^T (dK's A operand).
-            // -D per query, pairs of adjacent queries as one 64-bit value (16-byte
-            // loads); the first chunk's are read before the wait for dP^T
-            const ulonglong2* nd4 = reinterpret_cast<const ulonglong2*>(dvec_s + st * 128 + kQC * h);
-            ulonglong2 nd0[8];
-            if (ok) {
+                // dQ drain: this warpgroup's D/2 columns -> fp32 tiles -> bulk reduce-add
+                if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_dq, gs & 1, wd, kSiteDrain));
+                uint8_t* stage = smem + L::kStage0 + st * L::kStageBytes;
+                uint32_t acc[kDrainChunks][16];
+                if (ok) {
+                    tc_fence_after();
 #pragma unroll
-                for (int i = 0; i < 8; ++i) nd0[i] = nd4[i];
+                    for (int b = 0; b < kDrainChunks; ++b) tmem_ld16(tDQ + 16 * b, acc[b]);
+#pragma unroll
+                    for (int b = 0; b < kDrainChunks; ++b) tmem_ld_wait(acc[b]);
+                    tc_fence_before();
+                    mbar_arrive(bar_dr);
+                    // stage fp32 boxes of [128 x 32] over this step's Q (the first half of the
+                    // warpgroups, dQ columns [0, D/2)) and dO (the second half): dO is free
+                    // (dV, dP^T done before dQ), Q once dK is
+                    if (h < NWG / 2) ok = __all_sync(FULL, mbar_wait_sleep(bar_dk, gs & 1, wd, kSiteDrain));
+                } else {
+                    mbar_arrive(bar_dr);
+                }
+                if (ok) {
+#pragma unroll
+                    for (int b = 0; b < kDrainChunks; ++b) {
+                        // columns h kDC + 16 b ..: box (32 columns) and first 16-byte chunk in it
+                        const int col = h * kDC + 16 * b;
+                        uint8_t* box = stage + (col / 32) * L::kBox + r * 128;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            *reinterpret_cast<uint4*>(box + ((((col % 32) / 4 + j) ^ (r & 7)) << 4)) =
+                                make_uint4(acc[b][4 * j], acc[b][4 * j + 1], acc[b][4 * j + 2],
+                                           acc[b][4 * j + 3]);
+                    }
+                    fence_async_shared();
+                }
+                mbar_arrive(h >= NWG / 2 ? bar_sgd : bar_sgq);  // the reducer adds the staged tiles into dQ
             }
-            if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_dp, s & 1, wd, kSiteDsDP) &&
-                                              (s == 0 || mbar_wait_sleep(L::kDSInTmem ? bar_dq : bar_dk, (s - 1) & 1, wd,
-                                                                         kSiteDsDQ)));
+            // dK = tau * dK_acc and dV (this warpgroup's D/2 columns), staged over the K
+            // and V tiles, which no MMA reads any more: the commit after the last dK
+            // covers every MMA of this CTA (warpgroup 1 has not waited for it yet).  The
+            // persistent kernel stages them apart (the next item's MMAs may be running);
+            // its next item's first dV and dK MMAs wait for this warpgroup's arrivals
+            // after these reads.
+            if (ok && isteps > 0)
+                ok = __all_sync(FULL, mbar_wait_sleep(bar_dk, (gs - 1) & 1, wd, kSiteDrain));
+            if constexpr (PERSIST) {
+                // the previous item's dK/dV store has read the staging area (thread 0
+                // issued it and went on without waiting)
+                if (threadIdx.x == 0) bulk_wait_read<0>();
+                named_bar_sync(5, kEW);
+            }
             if (ok) {
                 tc_fence_after();
+                const uint32_t tDV = tmem + lane_off + L::kTmDV, tDK = tmem + lane_off + L::kTmDK;
 #pragma unroll
-                for (int c = 0; c < kQC / 32; ++c) {
-                    uint32_t dp[32], pk[16];
-                    tmem_ld32(tDP + 32 * c, dp);
-                    if (c == 0) {
+                for (int which = 0; which < 2; ++which) {
+                    uint8_t* dst = smem + (PERSIST ? L::kStageKV + (which ? L::kTile : 0) : (which ? L::kK : L::kV));
+                    const float scale = which ? p.tau : 1.f;
+                    const uint32_t src = which ? tDK : tDV;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) pk[i] = pkeep[i];
-                    } else {
-                        tmem_ld16(tS + 16 * c, pk);
-                        tmem_ld_wait(pk);
-                    }
-                    tmem_ld_wait(dp);
-                    uint32_t ds[16];
-                    ulonglong2 nd[8];
+                    for (int cc = 0; cc < kDC; cc += 16) {
+                        const int c0 = h * kDC + cc;
+                        uint32_t o[16];
+                        if (!SPARSE || isteps > 0) {
+                            tmem_ld16(src + c0, o);
+                            tmem_ld_wait(o);
+                        } else {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) nd[i] = c == 0 ? nd0[i] : nd4[8 * c + i];
+                            for (int i = 0; i < 16; ++i) o[i] = 0u;  // no query sees these keys
+                        }
+                        const int box = c0 / 64;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const uint64_t ndq = (i & 1) ? nd[i >> 1].y : nd[i >> 1].x;
-                        // dP - D in fp32, rounded to bf16, times the bf16 P
-                        const float2 t = f2_unpack(
-                            fadd2(f2_pack(u2f(dp[2 * i]), u2f(dp[2 * i + 1])), ndq));
-                        ds[i] = mul_bf16x2(pk[i], pack_bf16(t.x, t.y));
-                    }
-                    if constexpr (L::kDSInTmem) tmem_st16(tS + kQC / 2 + 16 * c, ds);
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const int chunk = ds_chunk0 + 4 * c + q4;
-                        *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
-                            make_uint4(ds[4 * q4], ds[4 * q4 + 1], ds[4 * q4 + 2], ds[4 * q4 + 3]);
+                        for (int q = 0; q < 2; ++q) {
+                            const int chunk = (c0 % 64) / 8 + q;
+                            uint4 v;
+                            v.x = pack_bf16(u2f(o[8 * q + 0]) * scale, u2f(o[8 * q + 1]) * scale);
+                            v.y = pack_bf16(u2f(o[8 * q + 2]) * scale, u2f(o[8 * q + 3]) * scale);
+                            v.z = pack_bf16(u2f(o[8 * q + 4]) * scale, u2f(o[8 * q + 5]) * scale);
+                            v.w = pack_bf16(u2f(o[8 * q + 6]) * scale, u2f(o[8 * q + 7]) * scale);
+                            *reinterpret_cast<uint4*>(dst + box * L::kBox + r * 128 +
+                                                      ((chunk ^ (r & 7)) << 4)) = v;
+                        }
                     }
                 }
                 fence_async_shared();
-                if constexpr (L::kDSInTmem) tmem_st_wait();
-                tc_fence_before();
             }
-            mbar_arrive(bar_ds);
-
-            // dQ drain: this warpgroup's D/2 columns -> fp32 tiles -> bulk reduce-add
-            if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_dq, s & 1, wd, kSiteDrain));
-            uint8_t* stage = smem + L::kStage0 + st * L::kStageBytes;
-            uint32_t acc[kDrainChunks][16];
-            if (ok) {
-                tc_fence_after();
-#pragma unroll
-                for (int b = 0; b < kDrainChunks; ++b) tmem_ld16(tDQ + 16 * b, acc[b]);
-#pragma unroll
-                for (int b = 0; b < kDrainChunks; ++b) tmem_ld_wait(acc[b]);
-                tc_fence_before();
-                mbar_arrive(bar_dr);
-                // stage fp32 boxes of [128 x 32] over this step's Q (the first half of the
-                // warpgroups, dQ columns [0, D/2)) and dO (the second half): dO is free
-                // (dV, dP^T done before dQ), Q once dK is
-                if (h < NWG / 2) ok = __all_sync(FULL, mbar_wait_sleep(bar_dk, s & 1, wd, kSiteDrain));
-            } else {
-                mbar_arrive(bar_dr);
-            }
-            if (ok) {
-#pragma unroll
-                for (int b = 0; b < kDrainChunks; ++b) {
-                    // columns h kDC + 16 b ..: box (32 columns) and first 16-byte chunk in it
-                    const int col = h * kDC + 16 * b;
-                    uint8_t* box = stage + (col / 32) * L::kBox + r * 128;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        *reinterpret_cast<uint4*>(box + ((((col % 32) / 4 + j) ^ (r & 7)) << 4)) =
-                            make_uint4(acc[b][4 * j], acc[b][4 * j + 1], acc[b][4 * j + 2],
-                                       acc[b][4 * j + 3]);
+            named_bar_sync(4, kEW);
+            if (threadIdx.x == 0 && ok) {
+                const uint32_t sv = sbase + (PERSIST ? L::kStageKV : L::kV);
+                const uint32_t sk = sbase + (PERSIST ? L::kStageKV + L::kTile : L::kK);
+                for (int b = 0; b < L::kBoxes; ++b) {
+                    tma_store_3d(&tmdV, sv + b * L::kBox, b * 64, kvs, ibh);
+                    tma_store_3d(&tmdK, sk + b * L::kBox, b * 64, kvs, ibh);
                 }
-                fence_async_shared();
+                bulk_commit();
+                if (!PERSIST) bulk_wait_read<0>();
             }
-            mbar_arrive(h >= NWG / 2 ? bar_sgd : bar_sgq);  // the reducer adds the staged tiles into dQ
         }
-        // dK = tau * dK_acc and dV (this warpgroup's D/2 columns), staged over the K
-        // and V tiles, which no MMA reads any more: the commit after the last dK
-        // covers every MMA of this CTA (warpgroup 1 has not waited for it yet)
-        if (ok && n_steps > 0)
-            ok = __all_sync(FULL, mbar_wait_sleep(bar_dk, (n_steps - 1) & 1, wd, kSiteDrain));
-        if (ok) {
-            tc_fence_after();
-            const uint32_t tDV = tmem + lane_off + L::kTmDV, tDK = tmem + lane_off + L::kTmDK;
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                uint8_t* dst = smem + (which ? L::kK : L::kV);
-                const float scale = which ? p.tau : 1.f;
-                const uint32_t src = which ? tDK : tDV;
-#pragma unroll
-                for (int cc = 0; cc < kDC; cc += 16) {
-                    const int c0 = h * kDC + cc;
-                    uint32_t o[16];
-                    if (!SPARSE || n_steps > 0) {
-                        tmem_ld16(src + c0, o);
-                        tmem_ld_wait(o);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) o[i] = 0u;  // no query sees these keys
-                    }
-                    const int box = c0 / 64;
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const int chunk = (c0 % 64) / 8 + q;
-                        uint4 v;
-                        v.x = pack_bf16(u2f(o[8 * q + 0]) * scale, u2f(o[8 * q + 1]) * scale);
-                        v.y = pack_bf16(u2f(o[8 * q + 2]) * scale, u2f(o[8 * q + 3]) * scale);
-                        v.z = pack_bf16(u2f(o[8 * q + 4]) * scale, u2f(o[8 * q + 5]) * scale);
-                        v.w = pack_bf16(u2f(o[8 * q + 6]) * scale, u2f(o[8 * q + 7]) * scale);
-                        *reinterpret_cast<uint4*>(dst + box * L::kBox + r * 128 +
-                                                  ((chunk ^ (r & 7)) << 4)) = v;
-                    }
-                }
-            }
-            fence_async_shared();
-        }
-        named_bar_sync(4, kEW);
-        if (threadIdx.x == 0 && ok) {
-            for (int b = 0; b < L::kBoxes; ++b) {
-                tma_store_3d(&tmdV, sbase + L::kV + b * L::kBox, b * 64, kv_start, bh);
-                tma_store_3d(&tmdK, sbase + L::kK + b * L::kBox, b * 64, kv_start, bh);
-            }
-            bulk_commit();
-            bulk_wait_read<0>();
-        }
+        if (PERSIST && threadIdx.x == 0) bulk_wait_read<0>();  // the last item's store
     }
 
     // ------------------------------------------------------------ teardown --
@@ -838,8 +947,23 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         // d = 128: four elementwise warpgroups (32 query columns each); d = 64: two
         // (four measured 4-8% slower there)
         constexpr int NWG = D == 128 ? 4 : 2;
+        // short d = 64 problems without a mask, with more work items than SMs: the
+        // persistent kernel, so that one item's set-up, first loads and epilogue
+        // overlap the next's
+        constexpr bool kCanPersist = D == 64 && MASK == kMaskNone;
+        int sms = 0;
+        if (kCanPersist) {
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                return cudaGetLastError();
+        }
+        const long long items = static_cast<long long>(a.BH) * ((a.N + kBK - 1) / kBK);
+        const bool persist = kCanPersist && a.N <= kBwdPersistMaxN && items > sms;
         constexpr auto kern = &fa_bwd_main_kernel<D, CAUSAL, MASK, NWG>;
-        cudaError_t e = set_max_dyn_smem_once<kern>(L::kBytes);
+        constexpr auto kern_p = &fa_bwd_main_kernel<D, CAUSAL, MASK, NWG, kCanPersist>;
+        cudaError_t e = persist ? set_max_dyn_smem_once<kern_p>(L::kBytesPersist)
+                                : set_max_dyn_smem_once<kern>(L::kBytes);
         if (e != cudaSuccess) return e;
         BwdParams p;
         p.LSE = a.LSE;
@@ -854,10 +978,16 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         p.head_group = bwd_head_group(a.BH, a.N, D, CAUSAL, MASK);
         p.err = a.err;
         p.wait_limit_ns = a.wait_limit_ns;
+        p.BH = a.BH;
+        if (items > (1ll << 30)) return cudaErrorInvalidValue;
+        p.items = static_cast<int>(items);
         dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(p.n_kv));
+        if (persist) grid = dim3(static_cast<unsigned>(sms));
         if (a.ev_start) cudaEventRecord(a.ev_start, stream);
-        e = launch_dependent(kern, grid, dim3(bwd_threads(NWG)), L::kBytes, stream, tq, tk, tv, tdo,
-                             tacc, tdk, tdv, p);
+        e = persist ? launch_dependent(kern_p, grid, dim3(bwd_threads(NWG)), L::kBytesPersist, stream, tq, tk,
+                                       tv, tdo, tacc, tdk, tdv, p)
+                    : launch_dependent(kern, grid, dim3(bwd_threads(NWG)), L::kBytes, stream, tq, tk, tv, tdo,
+                                       tacc, tdk, tdv, p);
         if (e == cudaSuccess && a.ev_stop) e = cudaEventRecord(a.ev_stop, stream);
         if (e != cudaSuccess) return e;
     }
