@@ -152,8 +152,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // softmax runs from block to block without waiting for P V and the next S
     constexpr bool PIPE = D == 64 && MASK == kMaskNone;
     // the row sums as paired fp32 adds (bitwise the same sums): measured faster
-    // in the one-tile kernel, slower in the two-tile one (register pressure)
-    constexpr bool PAIRED_SUMS = (PIPE && TILES == 1) || (D == 128 && MASK == kMaskNone && !O32);
+    // in the one-tile kernel, slower in the two-tile one (register pressure),
+    // except at d = 128 with a bf16 O (the sliding-window kernel too: 5% faster,
+    // and its spills are gone)
+    constexpr bool PAIRED_SUMS = (PIPE && TILES == 1) || (D == 128 && MASK != kMaskBlocks && !O32);
     // P is converted and stored in chunks of kPC packed columns: 16 at d = 128, which
     // frees the registers the paired sums need there, 32 at d = 64 and for the fp32
     // O (measured faster, and without spills, there)
