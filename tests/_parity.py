@@ -39,7 +39,7 @@ def bf16_floor(ref):
     ref = np64(ref)
     if ref.size == 0:
         return 0.0
-    return float(np.abs(torch.from_numpy(ref).to(torch.bfloat16).double().numpy() - ref).max())
+    return float(np.abs(torch.from_numpy(np.array(ref)).to(torch.bfloat16).double().numpy() - ref).max())
 
 
 def check_o(o, o_ref, bf16_out=True, what="O"):
