@@ -4,6 +4,7 @@ No compute call is made here (these run without a GPU)."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -13,8 +14,13 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "fa.h")
 
 
+def _read(path):
+    with open(path) as f:
+        return f.read()
+
+
 def declared_symbols():
-    text = open(HEADER).read()
+    text = _read(HEADER)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
 
@@ -36,7 +42,8 @@ def test_library_loads_and_exports_every_declared_symbol():
 
 def test_no_undeclared_exports():
     # the .so exports only the C ABI (hidden visibility for everything else)
-    out = os.popen(f"nm -D --defined-only {_lib.library_path()}").read()
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.library_path()], capture_output=True, text=True,
+                         check=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
     fa_syms = {s for s in exported if s.startswith("fa_")}
     assert fa_syms == set(declared_symbols())
@@ -126,7 +133,7 @@ def test_watchdog_selftest_rejects_bad_limits():
 def test_product_and_oracle_share_no_code():
     """The CUDA library never imports or links the oracle, and the oracle
     includes nothing from the library."""
-    out = os.popen(f"nm -D {_lib.library_path()}").read()
+    out = subprocess.run(["nm", "-D", _lib.library_path()], capture_output=True, text=True, check=True).stdout
     assert "ora_" not in out
     pkg = os.path.join(ROOT, "exact_io_aware_12_gb300")
     for dirpath, _, files in os.walk(pkg):
@@ -134,19 +141,19 @@ def test_product_and_oracle_share_no_code():
             continue
         for f in files:
             if f.endswith((".py", ".cu", ".cuh", ".h")):
-                text = open(os.path.join(dirpath, f)).read()
+                text = _read(os.path.join(dirpath, f))
                 assert not re.search(r"^\s*(import|from)\s+oracle", text, re.M), f
                 assert "ref_attn" not in text and "liboracle" not in text, f
     for f in os.listdir(os.path.join(ROOT, "oracle")):
         if f.endswith((".py", ".c", ".h")):
-            text = open(os.path.join(ROOT, "oracle", f)).read()
+            text = _read(os.path.join(ROOT, "oracle", f))
             assert not re.search(r"^\s*(import|from)\s+exact_io_aware_12_gb300", text, re.M), f
             assert "#include \"" not in text and "csrc" not in text, f
 
 
 def _header_define(name):
     """Value of an integer #define in include/fa.h (products of unsigned literals)."""
-    m = re.search(rf"#define\s+{name}\s+\(?([0-9u\s*]+)\)?", open(HEADER).read())
+    m = re.search(rf"#define\s+{name}\s+\(?([0-9u\s*]+)\)?", _read(HEADER))
     assert m, name
     value = 1
     for factor in m.group(1).split("*"):

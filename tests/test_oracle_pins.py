@@ -34,7 +34,8 @@ def _arr(x):
 
 # ---------------------------------------------------------------- golden ----
 def _golden_cases():
-    doc = json.load(open(os.path.join(HERE, "golden", "hand_worked.json")))
+    with open(os.path.join(HERE, "golden", "hand_worked.json")) as f:
+        doc = json.load(f)
     for case in doc["cases"]:
         for mode in ("noncausal", "causal", "windowed"):
             if mode in case:
