@@ -58,7 +58,8 @@ MUTANTS = {
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_planted_mistake(name, tmp_path):
     old, new = MUTANTS[name]
-    src = open(SRC).read()
+    with open(SRC) as f:
+        src = f.read()
     assert src.count(old) >= 1, f"mutation anchor not found: {old}"
     mutated = src.replace(old, new, 1)
     cfile = tmp_path / "ref_attn_mutant.c"

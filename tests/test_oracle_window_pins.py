@@ -80,8 +80,9 @@ def _blocked_window(q, k, v, tau, w, Br, Bc):
             seen = np.isfinite(blk)
             Pb = np.where(seen[:, None], np.exp(S - np.where(seen, blk, 0)[:, None]), 0.0)
             new_m = np.maximum(m[rows], blk)
-            a_old = np.where(np.isfinite(m[rows]), np.exp(m[rows] - new_m), 0.0)
-            a_blk = np.where(seen, np.exp(blk - new_m), 0.0)
+            with np.errstate(invalid="ignore"):  # -inf - -inf on rows the where() discards
+                a_old = np.where(np.isfinite(m[rows]), np.exp(m[rows] - new_m), 0.0)
+                a_blk = np.where(seen, np.exp(blk - new_m), 0.0)
             new_l = a_old * l[rows] + a_blk * Pb.sum(axis=1)
             num = l[rows, None] * a_old[:, None] * O[rows] + a_blk[:, None] * (Pb @ vj)
             # a row with no visible key so far keeps O = 0, l = 0 (nothing to normalise)
