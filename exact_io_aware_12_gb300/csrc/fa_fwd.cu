@@ -210,6 +210,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mbar_init(bar_o + 8 * t, 1);
         }
         mbar_init_fence();
+        if constexpr (SPARSE && TILES == 1) {
+            // the query tile is needed unless its mask row is empty: load it now, so
+            // that its latency overlaps the mask read below
+            mbar_arrive_expect_tx(bar_q, L::kTileBytes);
+            for (int b = 0; b < L::kBoxes; ++b)
+                tma_load_3d(sbase + L::kQ0 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start0, bh);
+        }
     }
     if (warp == kMmaWarp) {
         tmem_alloc(smem_addr(&sh.tmem_base), L::kTmemCols);
@@ -227,15 +234,27 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // below the diagonal when causal); one ballot per 32 blocks
             const uint8_t* m = p.blocks + bh * p.blocks_head_stride;
             const int qb[2] = {q_start0 / kBN, q_start1 / kBN};
-            for (int w = 0; w * 32 < n_kv; ++w) {
-                const int j = w * 32 + lane;
+            // eight 32-block words at a time: all their loads are in flight before
+            // the first ballot
+            for (int w0 = 0; w0 * 32 < n_kv; w0 += 8) {
+                bool u[8][2];
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    bool u = false;
-                    if ((t == 0 || q_start1 < N) && j < n_kv && (!CAUSAL || j <= qb[t]))
-                        u = m[static_cast<long long>(qb[t]) * n_kv + j] != 0;
-                    const uint32_t bits = __ballot_sync(0xffffffffu, u);
-                    if (lane == 0) sh.use[t][w] = bits;
+                for (int i = 0; i < 8; ++i) {
+                    const int j = (w0 + i) * 32 + lane;
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        u[i][t] = false;
+                        if ((t == 0 || q_start1 < N) && j < n_kv && (!CAUSAL || j <= qb[t]))
+                            u[i][t] = m[static_cast<long long>(qb[t]) * n_kv + j] != 0;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const uint32_t bits = __ballot_sync(0xffffffffu, u[i][t]);
+                        if (lane == 0 && (w0 + i) * 32 < n_kv) sh.use[t][w0 + i] = bits;
+                    }
                 }
             }
         }
@@ -266,14 +285,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             // with a block mask, a tile that visits no key block loads no Q, and a
             // pair that visits none loads nothing
             if (lane == 0 && (!SPARSE || nb > 0)) {
-                const bool q0 = !SPARSE || n_blk0 > 0;
-                uint32_t qbytes = L::kTileBytes * (q0 + (n_blk1 > 0));
-                mbar_arrive_expect_tx(bar_q, qbytes);
-                for (int b = 0; b < L::kBoxes; ++b) {
-                    if (q0)
-                        tma_load_3d(sbase + L::kQ0 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start0, bh);
-                    if (n_blk1 > 0)
-                        tma_load_3d(sbase + L::kQ1 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start1, bh);
+                if (!(SPARSE && TILES == 1)) {  // (the one-tile block-mask kernel loaded Q at the start)
+                    const bool q0 = !SPARSE || n_blk0 > 0;
+                    uint32_t qbytes = L::kTileBytes * (q0 + (n_blk1 > 0));
+                    mbar_arrive_expect_tx(bar_q, qbytes);
+                    for (int b = 0; b < L::kBoxes; ++b) {
+                        if (q0)
+                            tma_load_3d(sbase + L::kQ0 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start0, bh);
+                        if (n_blk1 > 0)
+                            tma_load_3d(sbase + L::kQ1 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start1, bh);
+                    }
                 }
                 int jb = -1;  // block mask: the block being loaded
                 for (int ld = 0; ld < 2 * nb; ++ld) {
@@ -743,19 +764,24 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         bool empty_tile = false;
         if constexpr (SPARSE) {
             // a tile whose mask row visits no key block: every row is the empty
-            // sum, O = 0 and LSE = -inf (its Q smem was never loaded: stage zeros there)
+            // sum, O = 0 and LSE = -inf, staged as zeros over its Q buffer (the one-tile
+            // kernel loaded Q all the same: that copy must land first)
             empty_tile = nbt == 0 && q_start < N;
             if (empty_tile) {
-                uint8_t* stage = smem + (t ? L::kQ1 : L::kQ0);
+                bool q_in = true;
+                if constexpr (TILES == 1) q_in = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteEpi));
+                if (q_in) {
+                    uint8_t* stage = smem + (t ? L::kQ1 : L::kQ0);
 #pragma unroll
-                for (int b = 0; b < L::kBoxes; ++b)
+                    for (int b = 0; b < L::kBoxes; ++b)
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(stage + b * L::kBoxBytes + r * 128 + c * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                fence_async_shared();
-                if (row < N) p.LSE[static_cast<int64_t>(bh) * N + row] = -INFINITY;
-                epi = true;
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4*>(stage + b * L::kBoxBytes + r * 128 + c * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                    fence_async_shared();
+                    if (row < N) p.LSE[static_cast<int64_t>(bh) * N + row] = -INFINITY;
+                }
+                epi = q_in;
             }
         }
         if (!O32 && (nbt > 0 || empty_tile)) {
