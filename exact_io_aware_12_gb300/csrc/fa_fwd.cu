@@ -44,8 +44,9 @@ constexpr int kBN = 128;  // keys per block
 // TILES = 2 (the default): two query tiles per CTA, 10 warps, all 512 tensor-
 // memory columns, one CTA per SM.  TILES = 1: one tile, 6 warps, 256 columns
 // and a smaller ring (5 slots at d = 64, 2 at d = 128), so two CTAs share an SM
-// and one's prologue and epilogue overlap the other's main loop: used where a
-// CTA has little work (d = 64 short sequences, block masks).
+// and one's prologue and epilogue overlap the other's main loop: used for d = 64
+// block masks (d = 64 short sequences and d = 128 block masks have persistent
+// kernels of their own, fa_fwd_short.cu and fa_fwd_sparse.cu).
 constexpr int threads_for(int tiles) { return tiles == 2 ? 320 : 192; }
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.44269504088896341f;
@@ -845,13 +846,12 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
-    if (a.blocks) {  // one tile per CTA: a block mask leaves each CTA little work
+    if (a.blocks) {  // a block mask leaves each query tile little work: one tile per CTA or item
         if (a.o32) return cudaErrorInvalidValue;
         if (a.d == 64)
             return a.causal ? launch_fwd_t<64, true, false, kMaskBlocks, 1>(a, stream)
                             : launch_fwd_t<64, false, false, kMaskBlocks, 1>(a, stream);
-        return a.causal ? launch_fwd_t<128, true, false, kMaskBlocks, 1>(a, stream)
-                        : launch_fwd_t<128, false, false, kMaskBlocks, 1>(a, stream);
+        return launch_fwd_sparse(a, stream);  // persistent, fa_fwd_sparse.cu
     }
     if (a.causal && !a.o32 && a.window > 0 && a.window < a.N)
         return a.d == 64 ? launch_fwd_t<64, true, false, kMaskWindow>(a, stream)

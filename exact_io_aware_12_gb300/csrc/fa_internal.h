@@ -144,6 +144,8 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 // d = 64, N <= 2048, bf16 O, no window or block mask: the persistent forward
 cudaError_t launch_fwd_short(const FwdArgs& a, cudaStream_t stream);
+// d = 128 with a block mask, bf16 O: the persistent block-sparse forward
+cudaError_t launch_fwd_sparse(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_fp8(const Fp8Args& a, cudaStream_t stream);
