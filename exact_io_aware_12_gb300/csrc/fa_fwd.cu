@@ -605,9 +605,24 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 const int last = CAUSAL ? min(row, N - 1) : N - 1;  // last visible key
                 if constexpr (LOCAL) {
                     const int first = row - window + 1;  // first visible key
+                    // a block is masked from above (diagonal, ragged end), from below (the
+                    // window's lower edge) or, with a short window, both: one compare per
+                    // score unless both
+                    const bool upper = (kbase + kBN - 1 > q_start) || (kbase + kBN > N);
+                    const bool lower = kbase <= q_start + kBM - 1 - window;
+                    if (upper && lower) {
 #pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        if (kbase + c > last || kbase + c < first) s[c >> 5][c & 31] = f2u(-INFINITY);
+                        for (int c = 0; c < 128; ++c)
+                            if (kbase + c > last || kbase + c < first) s[c >> 5][c & 31] = f2u(-INFINITY);
+                    } else if (lower) {
+#pragma unroll
+                        for (int c = 0; c < 128; ++c)
+                            if (kbase + c < first) s[c >> 5][c & 31] = f2u(-INFINITY);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 128; ++c)
+                            if (kbase + c > last) s[c >> 5][c & 31] = f2u(-INFINITY);
+                    }
                 } else {
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
