@@ -65,6 +65,30 @@ def _cases():
 CASES = _cases()
 
 
+def _persistent_cases():
+    """Shapes with more work items than CTAs for the persistent kernels: d = 64
+    dense (the short forward; the backward with more (key tile, head) items than
+    SMs) and d = 128 block masks (the block-sparse forward, more query tiles than
+    its two CTAs per SM)."""
+    g = np.random.default_rng(2027)
+    out = []
+    for i in range(6):
+        kind = ("dense", "blocks")[i % 2]
+        c = {"id": 100 + i, "kind": kind, "seed": 9100 + i, "causal": bool(g.integers(0, 2)),
+             "tau": float(g.uniform(0.04, 0.25)), "scale": float(g.choice([0.5, 1.0, 2.0]))}
+        if kind == "dense":
+            c.update(B=int(g.integers(2, 5)), H=int(g.integers(8, 13)), d=64, N=int(g.integers(1200, 2049)))
+        else:
+            c.update(B=2, H=int(g.integers(16, 25)), d=128, N=int(g.integers(1500, 2049)),
+                     density=float(g.uniform(0.1, 0.9)), per_head=bool(g.integers(0, 2)),
+                     empty_rows=int(g.integers(0, 2)))
+        out.append(c)
+    return out
+
+
+PERSISTENT_CASES = _persistent_cases()
+
+
 def _ids(c):
     shape = f"nq{c['Nq']}nk{c['Nk']}" if c["kind"] == "decode" else f"n{c['N']}"
     return f"{c['id']}-{c['kind']}-b{c['B']}h{c['H']}{shape}d{c['d']}{'c' if c['causal'] else ''}"
@@ -92,7 +116,7 @@ def _check_masked_fwd(o, lse, o_ref, l_ref):
         check_lse(l[~empty], l_ref[~empty])
 
 
-@pytest.mark.parametrize("c", CASES, ids=_ids)
+@pytest.mark.parametrize("c", CASES + PERSISTENT_CASES, ids=_ids)
 def test_random_case_matches_oracle(c):
     kind, B, H, d, causal, tau = c["kind"], c["B"], c["H"], c["d"], c["causal"], c["tau"]
     if kind == "fp8":
@@ -131,6 +155,8 @@ def test_random_case_matches_oracle(c):
         nb = (N + EDGE - 1) // EDGE
         heads = B * H if c["per_head"] else 1
         mask = random_block_mask(nb, heads, c["density"], c["seed"], empty_rows=c["empty_rows"])
+        if not c["per_head"]:
+            mask = mask[0]  # one [nb, nb] mask for every head
         kw_gpu["blocks"] = torch.from_numpy(np.ascontiguousarray(mask)).to(DEV)
         kw_ref["blocks"] = mask
     o, lse = api.fwd(q, k, v, causal, tau, **kw_gpu)
