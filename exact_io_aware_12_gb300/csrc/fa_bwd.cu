@@ -480,7 +480,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     tc_fence_after();
                     // d = 64: the dQ columns are reused every step
                     if (!L::kDQAliasDP && gs > 0) {
-                        if (!__all_sync(0xffffffffu, mbar_wait(bar_dr, (gs - 1) & 1, wd, kSiteMmaDrain))) { ok = false; break; }
+                        if (!__all_sync(0xffffffffu, mbar_wait(bar_dr, (gs - 1) & 1, wd, kSiteMmaDrain))) {
+                            ok = false;
+                            break;
+                        }
                         tc_fence_after();
                     }
                     // dQ first: its drain is on the elementwise warps' path; dK and the
@@ -501,7 +504,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                         // in the other buffer)
                         const int nkb = last_step ? (k + 1) & 1 : kb;
                         if (last_step) {
-                            if (!__all_sync(0xffffffffu, mbar_wait(bar_kv + 8 * nkb, ((k + 1) >> 1) & 1, wd, kSiteMmaKV))) {
+                            if (!__all_sync(0xffffffffu,
+                                            mbar_wait(bar_kv + 8 * nkb, ((k + 1) >> 1) & 1, wd, kSiteMmaKV))) {
                                 ok = false;
                                 break;
                             }
@@ -519,7 +523,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                         mma_commit_warp(bar_s);
                         // d = 128: dP^T over the dQ tile, once it has been read out
                         if (L::kDQAliasDP) {
-                            if (!__all_sync(0xffffffffu, mbar_wait(bar_dr, gs & 1, wd, kSiteMmaDrain))) { ok = false; break; }
+                            if (!__all_sync(0xffffffffu, mbar_wait(bar_dr, gs & 1, wd, kSiteMmaDrain))) {
+                                ok = false;
+                                break;
+                            }
                             tc_fence_after();
                         }
                         if (!__all_sync(0xffffffffu, mbar_wait(bar_df + 8 * st1, ((gs + 1) >> 1) & 1, wd, kSiteMmaQ))) {
@@ -695,9 +702,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
                     for (int i = 0; i < 8; ++i) nd0[i] = nd4[i];
                 }
-                if (ok) ok = __all_sync(FULL, mbar_wait_sleep(bar_dp, gs & 1, wd, kSiteDsDP) &&
-                                                  (gs == 0 || mbar_wait_sleep(L::kDSInTmem ? bar_dq : bar_dk, (gs - 1) & 1, wd,
-                                                                             kSiteDsDQ)));
+                if (ok)
+                    ok = __all_sync(FULL, mbar_wait_sleep(bar_dp, gs & 1, wd, kSiteDsDP) &&
+                                              (gs == 0 || mbar_wait_sleep(L::kDSInTmem ? bar_dq : bar_dk,
+                                                                          (gs - 1) & 1, wd, kSiteDsDQ)));
                 if (ok) {
                     tc_fence_after();
 #pragma unroll
