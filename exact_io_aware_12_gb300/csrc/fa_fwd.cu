@@ -28,7 +28,13 @@
 //     as soon as the softmax has read S (PIPE below);
 //   - causal: key blocks wholly above the diagonal are never loaded; the
 //     diagonal block is masked element-wise.  Keys >= N in a ragged last
-//     block are masked the same way.
+//     block are masked the same way;
+//   - d = 128 sliding windows run persistently when there are more tile pairs
+//     than SMs (PERSIST below): one CTA per SM walks a list of (batch*head,
+//     pair) items and keeps its barriers, tensor memory and K/V ring; the next
+//     item's Q tiles and first K/V blocks load while the current item's
+//     epilogue runs, and O is staged in a buffer of its own, so an item change
+//     costs only the epilogue.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -67,6 +73,10 @@ struct FwdLayout {
     static constexpr int kRing = TILES * kTileBytes;
     static constexpr int kBytes = kRing + kStages * kTileBytes;
     static constexpr int kDynSmem = kBytes + 1024;  // + alignment slack
+    // persistent kernel: O of tile t is staged 64 columns (one TMA box) at a time in
+    // a 16 KB area of its own, since Q_t is already loading the next item's tile
+    static constexpr int kOStage0 = kBytes, kOStage1 = kBytes + kBoxBytes;
+    static constexpr int kDynSmemPersist = kBytes + 2 * kBoxBytes + 1024;
     static constexpr uint32_t kTmemS0 = 0, kTmemS1 = TILES == 2 ? 128 : 0;
     static constexpr uint32_t kTmemO0 = TILES == 2 ? 256 : 128, kTmemO1 = TILES == 2 ? 256 + D : 128;
     static constexpr uint32_t kTmemCols = TILES == 2 ? 512 : 256;
@@ -78,6 +88,7 @@ struct FwdLayout {
 struct FwdParams {
     float* LSE;
     float* O32;
+    __nv_bfloat16* O16;  // PERSIST: O written from registers
     int N;
     int n_pairs;
     float scale_log2;  // tau * log2(e)
@@ -86,10 +97,14 @@ struct FwdParams {
     int window;  // causal sliding window in keys (0 = none)
     const uint8_t* blocks;          // block mask [heads][n_kv][n_kv] (kMaskBlocks)
     long long blocks_head_stride;   // bytes between heads' masks (0: one mask)
+    int BH;                         // PERSIST: batch*heads
+    int items;                      // PERSIST: work items (BH pairs each)
 };
 
 struct FwdShared {
     uint64_t q_full;
+    uint64_t q_empty;    // PERSIST: the item's MMAs are done; Q may take the next item's tiles
+    uint64_t o_free[2];  // PERSIST: the softmax warps have read O_t out (one phase per item)
     uint64_t kv_full[8];
     uint64_t kv_empty[8];
     uint64_t s_full[2];
@@ -104,7 +119,7 @@ struct FwdShared {
 // Wait-site ids recorded in the error word.
 enum : uint32_t {
     kSiteProdEmpty = 1, kSiteMmaQ = 2, kSiteMmaKV = 3, kSiteMmaP = 4,
-    kSiteSoftS = 5, kSiteSoftO = 6, kSiteEpi = 7
+    kSiteSoftS = 5, kSiteSoftO = 6, kSiteEpi = 7, kSiteProdQ = 8, kSiteMmaOF = 9
 };
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -137,9 +152,37 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint3
         mma_ts_warp<1>(tmem_o, tmem_p + k * 8, v_lo + ((k * 2048) >> 4), kDescHi, id);
 }
 
+// One work item: query tiles q_start0 and q_start1 (q_start1 = N, no second
+// tile, when TILES = 1) of head bh, and their key blocks [lo_t, hi_t): up to the
+// diagonal when causal, and from the block holding key (first row - window + 1)
+// with a sliding window.  The two ranges overlap or touch, so the loaders walk
+// [jlo, jlo + nb) without gaps.  (A block mask recounts n_blk0, n_blk1 and nb.)
+struct FwdItem {
+    int bh, q_start0, q_start1, lo0, lo1, hi0, hi1, n_blk0, n_blk1, jlo, nb;
+};
+
+template <bool CAUSAL, int TILES>
+__device__ __forceinline__ FwdItem fwd_item(int bh, int pair, int N, int n_kv, int window) {
+    FwdItem it;
+    it.bh = bh;
+    it.q_start0 = pair * TILES * kBM;
+    it.q_start1 = TILES == 2 ? it.q_start0 + kBM : N;
+    it.hi0 = CAUSAL ? min(n_kv, it.q_start0 / kBN + 1) : n_kv;
+    it.hi1 = it.q_start1 < N ? (CAUSAL ? min(n_kv, it.q_start1 / kBN + 1) : n_kv) : 0;
+    it.lo0 = window > 0 ? max(0, it.q_start0 - window + 1) / kBN : 0;
+    it.lo1 = window > 0 ? max(0, it.q_start1 - window + 1) / kBN : 0;
+    it.n_blk0 = it.hi0 - it.lo0;
+    it.n_blk1 = it.hi1 > 0 ? it.hi1 - it.lo1 : 0;
+    it.jlo = it.lo0;
+    it.nb = max(it.hi0, it.hi1) - it.jlo;
+    return it;
+}
+
 // MASK: kMaskNone; kMaskWindow, a causal sliding window of p.window keys (only
-// with CAUSAL); kMaskBlocks, the block mask p.blocks (bf16 O only).
-template <int D, bool CAUSAL, bool O32, int MASK, int TILES>
+// with CAUSAL); kMaskBlocks, the block mask p.blocks (bf16 O only).  PERSIST:
+// one CTA per SM walks a list of (batch*head, pair) items (d = 128, two tiles,
+// bf16 O, no block mask).
+template <int D, bool CAUSAL, bool O32, int MASK, int TILES, bool PERSIST = false>
 __global__ void __launch_bounds__(threads_for(TILES), TILES == 2 ? 1 : 2)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -152,6 +195,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // j + 1 is issued as soon as the softmax has read S of block j, and the
     // softmax runs from block to block without waiting for P V and the next S
     constexpr bool PIPE = D == 64 && MASK == kMaskNone;
+    static_assert(!PERSIST || (D == 128 && TILES == 2 && !O32 && !SPARSE),
+                  "persistent: d = 128 pairs, bf16 O");
     // the row sums as paired fp32 adds (bitwise the same sums): measured faster
     // in the one-tile kernel, slower in the two-tile one (register pressure),
     // except at d = 128 with a bf16 O (the sliding-window kernel too: 5% faster,
@@ -170,26 +215,44 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.y);  // heaviest pairs first
     const int N = p.N;
     const int n_kv = (N + kBN - 1) / kBN;
-    const int q_start0 = pair * TILES * kBM;
-    const int q_start1 = TILES == 2 ? q_start0 + kBM : N;  // TILES = 1: no second tile
-    // Key blocks [lo_t, hi_t) of tile t: up to the diagonal when causal, and from
-    // the block holding key (first row - window + 1) with a sliding window.  The
-    // two ranges overlap or touch, so the loaders walk [jlo, jhi) without gaps.
     const int window = (CAUSAL && LOCAL) ? p.window : 0;
-    const int hi0 = CAUSAL ? min(n_kv, q_start0 / kBN + 1) : n_kv;
-    const int hi1 = q_start1 < N ? (CAUSAL ? min(n_kv, q_start1 / kBN + 1) : n_kv) : 0;
-    const int lo0 = window > 0 ? max(0, q_start0 - window + 1) / kBN : 0;
-    const int lo1 = window > 0 ? max(0, q_start1 - window + 1) / kBN : 0;
-    int n_blk0 = hi0 - lo0;
-    int n_blk1 = hi1 > 0 ? hi1 - lo1 : 0;
-    const int jlo = lo0;
-    int nb = max(hi0, hi1) - jlo;  // key blocks loaded (with a block mask: counted below)
+    // Work items in launch order (x, the batch*head, fastest; the pair index y
+    // from the heaviest pair down): i = y BH + x.  Without PERSIST a CTA has one
+    // item, its launch position.  With PERSIST, CTA c of G takes items c,
+    // 2G - 1 - c, 2G + c, ... (a snake that balances heavy and light pairs
+    // without a shared counter).
+    auto item_of = [&](long long i) {
+        const int y = static_cast<int>(i / p.BH);
+        return fwd_item<CAUSAL, TILES>(static_cast<int>(i - static_cast<long long>(y) * p.BH),
+                                       p.n_pairs - 1 - y, N, n_kv, window);
+    };
+    FwdItem it0 = PERSIST ? item_of(blockIdx.x)
+                          : fwd_item<CAUSAL, TILES>(blockIdx.x, p.n_pairs - 1 - static_cast<int>(blockIdx.y),
+                                                    N, n_kv, window);
+    const int bh = it0.bh;
+    const int q_start0 = it0.q_start0, q_start1 = it0.q_start1;
+    [[maybe_unused]] const int hi0 = it0.hi0, hi1 = it0.hi1, lo0 = it0.lo0, lo1 = it0.lo1, jlo = it0.jlo;
+    int n_blk0 = it0.n_blk0, n_blk1 = it0.n_blk1;
+    int nb = it0.nb;  // key blocks loaded (with a block mask: counted below)
+    // work item k of this CTA into it, or false past the last
+    auto item_at = [&](int k, FwdItem& it) -> bool {
+        if constexpr (PERSIST) {
+            const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+            const long long i = static_cast<long long>(k) * G + ((k & 1) ? G - 1 - c : c);
+            if (i >= p.items) return false;
+            it = item_of(i);
+            return true;
+        }
+        if (k > 0) return false;
+        it = it0;
+        return true;
+    };
 
     const uint32_t bar_q = smem_addr(&sh.q_full);
+    const uint32_t bar_qe = smem_addr(&sh.q_empty);
+    const uint32_t bar_of = smem_addr(&sh.o_free[0]);
     const uint32_t bar_kv_full = smem_addr(&sh.kv_full[0]);
     const uint32_t bar_kv_empty = smem_addr(&sh.kv_empty[0]);
     const uint32_t bar_s = smem_addr(&sh.s_full[0]);
@@ -209,7 +272,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mbar_init(bar_sf + 8 * t, 128);
             mbar_init(bar_p + 8 * t, 128);
             mbar_init(bar_o + 8 * t, 1);
+            mbar_init(bar_of + 8 * t, 128);
         }
+        mbar_init(bar_qe, 1);
         mbar_init_fence();
         if constexpr (SPARSE && TILES == 1) {
             // the query tile is needed unless its mask row is empty: load it now, so
@@ -278,48 +343,66 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         n_blk0 = c0;
         n_blk1 = c1;
         nb = cu;
+        it0.n_blk0 = c0;
+        it0.n_blk1 = c1;
+        it0.nb = cu;
     }
 
     if (warp >= kProducerWarp) {
         if (warp == kProducerWarp) {
             // ------------------------------------------------------- producer --
             // with a block mask, a tile that visits no key block loads no Q, and a
-            // pair that visits none loads nothing
-            if (lane == 0 && (!SPARSE || nb > 0)) {
-                if (!(SPARSE && TILES == 1)) {  // (the one-tile block-mask kernel loaded Q at the start)
-                    const bool q0 = !SPARSE || n_blk0 > 0;
-                    uint32_t qbytes = L::kTileBytes * (q0 + (n_blk1 > 0));
-                    mbar_arrive_expect_tx(bar_q, qbytes);
-                    for (int b = 0; b < L::kBoxes; ++b) {
-                        if (q0)
-                            tma_load_3d(sbase + L::kQ0 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start0, bh);
-                        if (n_blk1 > 0)
-                            tma_load_3d(sbase + L::kQ1 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, q_start1, bh);
+            // pair that visits none loads nothing.  Ring loads are numbered across
+            // the items (g): the slot and the barrier phases follow g.
+            if (lane == 0) {
+                bool pok = true;
+                int g0 = 0;  // ring loads of the earlier items
+                FwdItem it;
+                for (int k = 0; (PERSIST || k == 0) && pok && item_at(k, it); ++k) {
+                    if (SPARSE && it.nb == 0) break;
+                    // the Q buffers take this item's tiles once the previous item's MMAs are done
+                    if (PERSIST && k > 0 && !mbar_wait(bar_qe, (k - 1) & 1, wd, kSiteProdQ)) break;
+                    if (!(SPARSE && TILES == 1)) {  // (the one-tile block-mask kernel loaded Q at the start)
+                        const bool q0 = !SPARSE || it.n_blk0 > 0;
+                        uint32_t qbytes = L::kTileBytes * (q0 + (it.n_blk1 > 0));
+                        mbar_arrive_expect_tx(bar_q, qbytes);
+                        for (int b = 0; b < L::kBoxes; ++b) {
+                            if (q0)
+                                tma_load_3d(sbase + L::kQ0 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, it.q_start0,
+                                            it.bh);
+                            if (it.n_blk1 > 0)
+                                tma_load_3d(sbase + L::kQ1 + b * L::kBoxBytes, &tmQ, bar_q, b * 64, it.q_start1,
+                                            it.bh);
+                        }
                     }
-                }
-                int jb = -1;  // block mask: the block being loaded
-                for (int ld = 0; ld < 2 * nb; ++ld) {
-                    const int slot = ld % L::kStages;
-                    if (ld >= L::kStages &&
-                        !mbar_wait(bar_kv_empty + 8 * slot, ((ld / L::kStages) - 1) & 1, wd, kSiteProdEmpty))
-                        break;
-                    bool is_k = (ld & 1) == 0;
-                    int blk = jlo + (ld >> 1);
-                    if constexpr (PIPE) {
-                        // the MMA warp's order: K0 K1 V0 K2 V1 ... K(nb-1) V(nb-2) V(nb-1)
-                        is_k = ld == 0 || ((ld & 1) && ld < 2 * nb - 1);
-                        blk = is_k ? (ld + 1) / 2 : (ld == 2 * nb - 1 ? nb - 1 : ld / 2 - 1);
+                    int jb = -1;  // block mask: the block being loaded
+                    for (int ld = 0; ld < 2 * it.nb; ++ld) {
+                        const int g = g0 + ld;
+                        const int slot = g % L::kStages;
+                        if (g >= L::kStages &&
+                            !mbar_wait(bar_kv_empty + 8 * slot, ((g / L::kStages) - 1) & 1, wd, kSiteProdEmpty)) {
+                            pok = false;
+                            break;
+                        }
+                        bool is_k = (ld & 1) == 0;
+                        int blk = it.jlo + (ld >> 1);
+                        if constexpr (PIPE) {
+                            // the MMA warp's order: K0 K1 V0 K2 V1 ... K(nb-1) V(nb-2) V(nb-1)
+                            is_k = ld == 0 || ((ld & 1) && ld < 2 * it.nb - 1);
+                            blk = is_k ? (ld + 1) / 2 : (ld == 2 * it.nb - 1 ? it.nb - 1 : ld / 2 - 1);
+                        }
+                        const CUtensorMap* map = is_k ? &tmK : &tmV;
+                        const uint32_t dst = sbase + L::kRing + slot * L::kTileBytes;
+                        if constexpr (SPARSE) {
+                            if ((ld & 1) == 0) jb = next_set_bit(sh.use[0], sh.use[1], jb + 1, n_kv);
+                            blk = jb;
+                        }
+                        mbar_arrive_expect_tx(bar_kv_full + 8 * slot, L::kTileBytes);
+                        for (int b = 0; b < L::kBoxes; ++b)
+                            tma_load_3d(dst + b * L::kBoxBytes, map, bar_kv_full + 8 * slot, b * 64,
+                                        blk * kBN, it.bh);
                     }
-                    const CUtensorMap* map = is_k ? &tmK : &tmV;
-                    const uint32_t dst = sbase + L::kRing + slot * L::kTileBytes;
-                    if constexpr (SPARSE) {
-                        if ((ld & 1) == 0) jb = next_set_bit(sh.use[0], sh.use[1], jb + 1, n_kv);
-                        blk = jb;
-                    }
-                    mbar_arrive_expect_tx(bar_kv_full + 8 * slot, L::kTileBytes);
-                    for (int b = 0; b < L::kBoxes; ++b)
-                        tma_load_3d(dst + b * L::kBoxBytes, map, bar_kv_full + 8 * slot, b * 64,
-                                    blk * kBN, bh);
+                    g0 += 2 * it.nb;
                 }
             }
         } else if (warp == kMmaWarp) {
@@ -449,104 +532,138 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         }
                     }
                 } else {
-                    const int lo[2] = {lo0, lo1};
-                    const int hi[2] = {hi0, n_blk1 > 0 ? hi1 : 0};
-                    bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteMmaQ) &&
-                                                          mbar_wait(bar_kv_full, 0, wd, kSiteMmaKV));
-                    if (ok) {
-                        tc_fence_after();
-                        for (int t = 0; t < 2; ++t) {
-                            if (lo[t] == jlo && hi[t] > jlo) {
-                                issue_s<D>(tS[t], qlo[t], klo0);
-                                mma_commit_warp(bar_s + 8 * t);
-                            }
-                        }
-                        mma_commit_warp(bar_kv_empty);
-                    }
-                    if constexpr (!LOCAL) {
-                        // every tile starts at key block 0: tile t takes blocks [0, hi[t])
-                        for (int j = 0; ok && j < nb; ++j) {
-                            const int lv = 2 * j + 1, lk = 2 * j + 2;
-                            const int sv = lv % L::kStages, sk = lk % L::kStages;
-                            if (!__all_sync(0xffffffffu,
-                                            mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1, wd, kSiteMmaKV))) {
-                                ok = false;
-                                break;
-                            }
+                    // Ring loads (g), S_t / P_t / P_t V products (cb[t]) and Q fills
+                    // (k) are counted across the items; the barrier phases follow them.
+                    bool ok = true;
+                    int g0 = 0;            // ring loads of the earlier items
+                    int cb0 = 0, cb1 = 0;  // blocks of tile 0 / 1 in the earlier items
+                    FwdItem it;
+                    for (int k = 0; (PERSIST || k == 0) && ok && item_at(k, it); ++k) {
+                        const int lo[2] = {it.lo0, it.lo1};
+                        const int hi[2] = {it.hi0, it.n_blk1 > 0 ? it.hi1 : 0};
+                        const int cb[2] = {cb0, cb1};
+                        const int s0 = g0 % L::kStages;
+                        ok = __all_sync(0xffffffffu, mbar_wait(bar_q, k & 1, wd, kSiteMmaQ) &&
+                                                         mbar_wait(bar_kv_full + 8 * s0, (g0 / L::kStages) & 1, wd,
+                                                                   kSiteMmaKV));
+                        if (ok) {
                             tc_fence_after();
-                            bool k_ready = false;
-                            for (int t = 0; t < 2 && ok; ++t) {
-                                if (j >= hi[t]) continue;
-                                if (!__all_sync(0xffffffffu, mbar_wait(bar_p + 8 * t, j & 1, wd, kSiteMmaP))) {
+                            for (int t = 0; t < 2; ++t) {
+                                if (lo[t] == it.jlo && hi[t] > it.jlo) {
+                                    issue_s<D>(tS[t], qlo[t], klo0 + s0 * kSlot);
+                                    mma_commit_warp(bar_s + 8 * t);
+                                }
+                            }
+                            mma_commit_warp(bar_kv_empty + 8 * s0);
+                        }
+                        // before tile t's first P V of an item (accumulate = 0), the softmax
+                        // warps must have read the previous item's O_t out
+                        auto o_free_wait = [&](int t) -> bool {
+                            if (!PERSIST || k == 0) return true;
+                            const bool w = __all_sync(0xffffffffu,
+                                                      mbar_wait(bar_of + 8 * t, (k - 1) & 1, wd, kSiteMmaOF));
+                            if (w) tc_fence_after();
+                            return w;
+                        };
+                        if constexpr (!LOCAL) {
+                            // every tile starts at key block 0: tile t takes blocks [0, hi[t]).
+                            // Both tiles' O must be free before the first P V (tile 1's
+                            // epilogue ends about a block after tile 0's, while tile 0 runs
+                            // its first softmax): the block loop stays that of one item.
+                            if (ok) ok = o_free_wait(0) && (hi[1] == 0 || o_free_wait(1));
+                            for (int j = 0; ok && j < it.nb; ++j) {
+                                const int lv = g0 + 2 * j + 1, lk = g0 + 2 * j + 2;
+                                const int sv = lv % L::kStages, sk = lk % L::kStages;
+                                if (!__all_sync(0xffffffffu, mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1,
+                                                                       wd, kSiteMmaKV))) {
                                     ok = false;
                                     break;
                                 }
                                 tc_fence_after();
-                                issue_pv<D>(tO[t], tS[t], vlo0 + sv * kSlot, j > 0);
-                                mma_commit_warp(bar_o + 8 * t);
-                                if (j + 1 < hi[t]) {
-                                    if (!k_ready) {
-                                        if (!__all_sync(0xffffffffu,
-                                                        mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1,
-                                                                  wd, kSiteMmaKV))) {
-                                            ok = false;
-                                            break;
+                                bool k_ready = false;
+                                for (int t = 0; t < 2 && ok; ++t) {
+                                    if (j >= hi[t]) continue;
+                                    if (!__all_sync(0xffffffffu,
+                                                    mbar_wait(bar_p + 8 * t, (cb[t] + j) & 1, wd, kSiteMmaP))) {
+                                        ok = false;
+                                        break;
+                                    }
+                                    tc_fence_after();
+                                    issue_pv<D>(tO[t], tS[t], vlo0 + sv * kSlot, j > 0);
+                                    mma_commit_warp(bar_o + 8 * t);
+                                    if (j + 1 < hi[t]) {
+                                        if (!k_ready) {
+                                            if (!__all_sync(0xffffffffu,
+                                                            mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1,
+                                                                      wd, kSiteMmaKV))) {
+                                                ok = false;
+                                                break;
+                                            }
+                                            tc_fence_after();
+                                            k_ready = true;
                                         }
-                                        tc_fence_after();
-                                        k_ready = true;
-                                    }
-                                    issue_s<D>(tS[t], qlo[t], klo0 + sk * kSlot);
-                                    mma_commit_warp(bar_s + 8 * t);
-                                }
-                            }
-                            if (!ok) break;
-                            mma_commit_warp(bar_kv_empty + 8 * sv);
-                            if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
-                        }
-                    } else {
-                        // tile t takes blocks [lo[t], hi[t]); S of a tile's first block may
-                        // be issued while the other tile is still in its leading blocks
-                        for (int u = 0; ok && u < nb; ++u) {
-                            const int j = jlo + u;  // key block
-                            const int lv = 2 * u + 1, lk = 2 * u + 2;
-                            const int sv = lv % L::kStages, sk = lk % L::kStages;
-                            if (!__all_sync(0xffffffffu,
-                                            mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1, wd, kSiteMmaKV))) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            bool k_ready = false;
-                            // fully unrolled over the two tiles so the per-tile arrays stay in registers
-        #pragma unroll
-                            for (int t = 0; t < 2; ++t) {
-                                if (ok && j >= lo[t] && j < hi[t]) {
-                                    ok = __all_sync(0xffffffffu,
-                                                    mbar_wait(bar_p + 8 * t, (j - lo[t]) & 1, wd, kSiteMmaP));
-                                    if (ok) {
-                                        tc_fence_after();
-                                        issue_pv<D>(tO[t], tS[t], vlo0 + sv * kSlot, j > lo[t]);
-                                        mma_commit_warp(bar_o + 8 * t);
-                                    }
-                                }
-                                if (ok && j + 1 >= lo[t] && j + 1 < hi[t]) {
-                                    if (!k_ready) {
-                                        ok = __all_sync(0xffffffffu,
-                                                        mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1,
-                                                                  wd, kSiteMmaKV));
-                                        if (ok) tc_fence_after();
-                                        k_ready = true;
-                                    }
-                                    if (ok) {
                                         issue_s<D>(tS[t], qlo[t], klo0 + sk * kSlot);
                                         mma_commit_warp(bar_s + 8 * t);
                                     }
                                 }
+                                if (!ok) break;
+                                mma_commit_warp(bar_kv_empty + 8 * sv);
+                                if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
                             }
-                            if (!ok) break;
-                            mma_commit_warp(bar_kv_empty + 8 * sv);
-                            if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
+                        } else {
+                            // tile t takes blocks [lo[t], hi[t]); S of a tile's first block may
+                            // be issued while the other tile is still in its leading blocks
+                            for (int u = 0; ok && u < it.nb; ++u) {
+                                const int j = it.jlo + u;  // key block
+                                const int lv = g0 + 2 * u + 1, lk = g0 + 2 * u + 2;
+                                const int sv = lv % L::kStages, sk = lk % L::kStages;
+                                if (!__all_sync(0xffffffffu, mbar_wait(bar_kv_full + 8 * sv, (lv / L::kStages) & 1,
+                                                                       wd, kSiteMmaKV))) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                bool k_ready = false;
+                                // fully unrolled over the two tiles so the per-tile arrays stay in registers
+#pragma unroll
+                                for (int t = 0; t < 2; ++t) {
+                                    if (ok && j >= lo[t] && j < hi[t]) {
+                                        if (j == lo[t]) ok = o_free_wait(t);
+                                        if (ok)
+                                            ok = __all_sync(0xffffffffu,
+                                                            mbar_wait(bar_p + 8 * t, (cb[t] + j - lo[t]) & 1, wd,
+                                                                      kSiteMmaP));
+                                        if (ok) {
+                                            tc_fence_after();
+                                            issue_pv<D>(tO[t], tS[t], vlo0 + sv * kSlot, j > lo[t]);
+                                            mma_commit_warp(bar_o + 8 * t);
+                                        }
+                                    }
+                                    if (ok && j + 1 >= lo[t] && j + 1 < hi[t]) {
+                                        if (!k_ready) {
+                                            ok = __all_sync(0xffffffffu,
+                                                            mbar_wait(bar_kv_full + 8 * sk, (lk / L::kStages) & 1,
+                                                                      wd, kSiteMmaKV));
+                                            if (ok) tc_fence_after();
+                                            k_ready = true;
+                                        }
+                                        if (ok) {
+                                            issue_s<D>(tS[t], qlo[t], klo0 + sk * kSlot);
+                                            mma_commit_warp(bar_s + 8 * t);
+                                        }
+                                    }
+                                }
+                                if (!ok) break;
+                                mma_commit_warp(bar_kv_empty + 8 * sv);
+                                if (k_ready) mma_commit_warp(bar_kv_empty + 8 * sk);
+                            }
                         }
+                        // the Q tiles take the next item's once this item's MMAs are done
+                        // (committing right after the last S measured slower)
+                        if (PERSIST && ok) mma_commit_warp(bar_qe);
+                        g0 += 2 * it.nb;
+                        cb0 += it.n_blk0;
+                        cb1 += it.n_blk1;
                     }
                 }
             }
@@ -556,10 +673,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         // -------------------------------------------------------- softmax --
         const int t = warp >> 2;
         const int r = threadIdx.x & 127;
-        const int q_start = t ? q_start1 : q_start0;
-        const int nbt = t ? n_blk1 : n_blk0;
-        const int lot = t ? lo1 : lo0;
-        const int row = q_start + r;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_off + (t ? L::kTmemS1 : L::kTmemS0);
         const uint32_t tO = tmem + lane_off + (t ? L::kTmemO1 : L::kTmemO0);
@@ -568,252 +681,308 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const uint32_t my_s = bar_s + 8 * t, my_p = bar_p + 8 * t, my_o = bar_o + 8 * t;
         const uint32_t my_sf = bar_sf + 8 * t;
         const float sl2 = p.scale_log2;
-        float m_used = -INFINITY;
-        float l = 0.f, l_mma = 0.f;
         bool ok = true;
-        int jsp = -1;  // block mask: the last key block visited
-        for (int jj = 0; jj < nbt; ++jj) {
-            int j = lot + jj;  // key block
-            if constexpr (SPARSE) {
-                jsp = next_set_bit(sh.use[t], nullptr, jsp + 1, n_kv);
-                j = jsp;
-            }
-            // wait results are made warp-uniform: tcgen05.ld/st are warp-collective
-            if (!__all_sync(0xffffffffu, mbar_wait(my_s, jj & 1, wd, kSiteSoftS))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t s[4][32];
-            tmem_ld32(tS + 0, s[0]);
-            tmem_ld32(tS + 32, s[1]);
-            tmem_ld32(tS + 64, s[2]);
-            tmem_ld32(tS + 96, s[3]);
-            tmem_ld_wait(s[0]);
-            tmem_ld_wait(s[1]);
-            tmem_ld_wait(s[2]);
-            tmem_ld_wait(s[3]);
-            if constexpr (PIPE) {
-                tc_fence_before();
-                mbar_arrive(my_sf);  // S's columns may take the next block's scores now
-            }
+        int cbt = 0;  // this tile's blocks in the earlier items (barrier phases)
+        FwdItem it;
+        for (int k = 0; (k == 0 || (PERSIST && ok)) && item_at(k, it); ++k) {
+            const int ibh = it.bh;
+            const int q_start = t ? it.q_start1 : it.q_start0;
+            const int nbt = t ? it.n_blk1 : it.n_blk0;
+            const int lot = t ? it.lo1 : it.lo0;
+            const int row = q_start + r;
+            float m_used = -INFINITY;
+            float l = 0.f, l_mma = 0.f;
+            int jsp = -1;  // block mask: the last key block visited
+            for (int jj = 0; jj < nbt; ++jj) {
+                int j = lot + jj;  // key block
+                if constexpr (SPARSE) {
+                    jsp = next_set_bit(sh.use[t], nullptr, jsp + 1, n_kv);
+                    j = jsp;
+                }
+                // wait results are made warp-uniform: tcgen05.ld/st are warp-collective
+                if (!__all_sync(0xffffffffu, mbar_wait(my_s, (cbt + jj) & 1, wd, kSiteSoftS))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t s[4][32];
+                tmem_ld32(tS + 0, s[0]);
+                tmem_ld32(tS + 32, s[1]);
+                tmem_ld32(tS + 64, s[2]);
+                tmem_ld32(tS + 96, s[3]);
+                tmem_ld_wait(s[0]);
+                tmem_ld_wait(s[1]);
+                tmem_ld_wait(s[2]);
+                tmem_ld_wait(s[3]);
+                if constexpr (PIPE) {
+                    tc_fence_before();
+                    mbar_arrive(my_sf);  // S's columns may take the next block's scores now
+                }
 
-            const int kbase = j * kBN;
-            const bool need_mask = (CAUSAL && kbase + kBN - 1 > q_start) || (kbase + kBN > N) ||
-                                   (window > 0 && kbase <= q_start + kBM - 1 - window);
-            if (need_mask) {
-                const int last = CAUSAL ? min(row, N - 1) : N - 1;  // last visible key
-                if constexpr (LOCAL) {
-                    const int first = row - window + 1;  // first visible key
-                    // a block is masked from above (diagonal, ragged end), from below (the
-                    // window's lower edge) or, with a short window, both: one compare per
-                    // score unless both
-                    const bool upper = (kbase + kBN - 1 > q_start) || (kbase + kBN > N);
-                    const bool lower = kbase <= q_start + kBM - 1 - window;
-                    if (upper && lower) {
+                const int kbase = j * kBN;
+                const bool need_mask = (CAUSAL && kbase + kBN - 1 > q_start) || (kbase + kBN > N) ||
+                                       (window > 0 && kbase <= q_start + kBM - 1 - window);
+                if (need_mask) {
+                    const int last = CAUSAL ? min(row, N - 1) : N - 1;  // last visible key
+                    if constexpr (LOCAL) {
+                        const int first = row - window + 1;  // first visible key
+                        // a block is masked from above (diagonal, ragged end), from below (the
+                        // window's lower edge) or, with a short window, both: one compare per
+                        // score unless both
+                        const bool upper = (kbase + kBN - 1 > q_start) || (kbase + kBN > N);
+                        const bool lower = kbase <= q_start + kBM - 1 - window;
+                        if (upper && lower) {
 #pragma unroll
-                        for (int c = 0; c < 128; ++c)
-                            if (kbase + c > last || kbase + c < first) s[c >> 5][c & 31] = f2u(-INFINITY);
-                    } else if (lower) {
+                            for (int c = 0; c < 128; ++c)
+                                if (kbase + c > last || kbase + c < first) s[c >> 5][c & 31] = f2u(-INFINITY);
+                        } else if (lower) {
 #pragma unroll
-                        for (int c = 0; c < 128; ++c)
-                            if (kbase + c < first) s[c >> 5][c & 31] = f2u(-INFINITY);
+                            for (int c = 0; c < 128; ++c)
+                                if (kbase + c < first) s[c >> 5][c & 31] = f2u(-INFINITY);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 128; ++c)
+                                if (kbase + c > last) s[c >> 5][c & 31] = f2u(-INFINITY);
+                        }
                     } else {
 #pragma unroll
                         for (int c = 0; c < 128; ++c)
                             if (kbase + c > last) s[c >> 5][c & 31] = f2u(-INFINITY);
                     }
+                }
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    mx0 = fmax3(mx0, u2f(s[0][c]), u2f(s[0][c + 1]));
+                    mx1 = fmax3(mx1, u2f(s[1][c]), u2f(s[1][c + 1]));
+                    mx2 = fmax3(mx2, u2f(s[2][c]), u2f(s[2][c + 1]));
+                    mx3 = fmax3(mx3, u2f(s[3][c]), u2f(s[3][c + 1]));
+                }
+                const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+                const bool grow = m_cand > m_used + kRescaleThreshold;
+                float alpha = 1.f;
+                if (grow) {
+                    alpha = ex2(m_used - m_cand);  // 0 on the first block (m_used = -inf)
+                    m_used = m_cand;
+                }
+                // unmasked kernels round the row sums' rescale and update separately (no
+                // FMA contraction), so they and the persistent short forward give the
+                // same LSE bits
+                if constexpr (MASK == kMaskNone) {
+                    l = __fmul_rn(l, alpha);
+                    l_mma = __fmul_rn(l_mma, alpha);
                 } else {
-#pragma unroll
-                    for (int c = 0; c < 128; ++c)
-                        if (kbase + c > last) s[c >> 5][c & 31] = f2u(-INFINITY);
+                    l *= alpha;
+                    l_mma *= alpha;
                 }
-            }
-            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+                const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+                // Two row sums: l_mma over the bf16 P values the P.V MMA consumes (it
+                // normalises O, so the weights actually applied sum to one) and l over
+                // the fp32 values (it gives LSE).
+                // the scale-and-subtract runs as one paired fp32 FMA per two scores
+                const uint64_t c2 = f2_pack(sl2, sl2), nm2 = f2_pack(neg_m, neg_m);
+                float ls0 = 0.f, ls1 = 0.f, lr0 = 0.f, lr1 = 0.f;
+                uint64_t ls2 = 0, lr2 = 0;  // PAIRED_SUMS: the same sums, paired (bitwise equal)
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-                mx0 = fmax3(mx0, u2f(s[0][c]), u2f(s[0][c + 1]));
-                mx1 = fmax3(mx1, u2f(s[1][c]), u2f(s[1][c + 1]));
-                mx2 = fmax3(mx2, u2f(s[2][c]), u2f(s[2][c + 1]));
-                mx3 = fmax3(mx3, u2f(s[3][c]), u2f(s[3][c + 1]));
-            }
-            const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-            const bool grow = m_cand > m_used + kRescaleThreshold;
-            float alpha = 1.f;
-            if (grow) {
-                alpha = ex2(m_used - m_cand);  // 0 on the first block (m_used = -inf)
-                m_used = m_cand;
-            }
-            // unmasked kernels round the row sums' rescale and update separately (no
-            // FMA contraction), so they and the persistent short forward give the
-            // same LSE bits
-            if constexpr (MASK == kMaskNone) {
-                l = __fmul_rn(l, alpha);
-                l_mma = __fmul_rn(l_mma, alpha);
-            } else {
-                l *= alpha;
-                l_mma *= alpha;
-            }
-            const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
-            // Two row sums: l_mma over the bf16 P values the P.V MMA consumes (it
-            // normalises O, so the weights actually applied sum to one) and l over
-            // the fp32 values (it gives LSE).
-            // the scale-and-subtract runs as one paired fp32 FMA per two scores
-            const uint64_t c2 = f2_pack(sl2, sl2), nm2 = f2_pack(neg_m, neg_m);
-            float ls0 = 0.f, ls1 = 0.f, lr0 = 0.f, lr1 = 0.f;
-            uint64_t ls2 = 0, lr2 = 0;  // PAIRED_SUMS: the same sums, paired (bitwise equal)
+                for (int h = 0; h < 64 / kPC; ++h) {
+                    uint32_t pk[kPC];
 #pragma unroll
-            for (int h = 0; h < 64 / kPC; ++h) {
-                uint32_t pk[kPC];
-#pragma unroll
-                for (int i = 0; i < kPC; ++i) {
-                    const int c = h * 2 * kPC + 2 * i;
-                    const float2 x = f2_unpack(ffma2(
-                        f2_pack(u2f(s[c >> 5][c & 31]), u2f(s[c >> 5][(c & 31) + 1])), c2, nm2));
-                    const float p0 = ex2(x.x), p1 = ex2(x.y);
-                    pk[i] = pack_bf16(p0, p1);
-                    if constexpr (PAIRED_SUMS) {
-                        ls2 = fadd2(ls2, f2_pack(p0, p1));
-                        lr2 = fadd2(lr2, f2_pack(u2f(pk[i] << 16), u2f(pk[i] & 0xffff0000u)));
-                    } else {
-                        ls0 += p0;
-                        ls1 += p1;
-                        lr0 += u2f(pk[i] << 16);
-                        lr1 += u2f(pk[i] & 0xffff0000u);
+                    for (int i = 0; i < kPC; ++i) {
+                        const int c = h * 2 * kPC + 2 * i;
+                        const float2 x = f2_unpack(ffma2(
+                            f2_pack(u2f(s[c >> 5][c & 31]), u2f(s[c >> 5][(c & 31) + 1])), c2, nm2));
+                        const float p0 = ex2(x.x), p1 = ex2(x.y);
+                        pk[i] = pack_bf16(p0, p1);
+                        if constexpr (PAIRED_SUMS) {
+                            ls2 = fadd2(ls2, f2_pack(p0, p1));
+                            lr2 = fadd2(lr2, f2_pack(u2f(pk[i] << 16), u2f(pk[i] & 0xffff0000u)));
+                        } else {
+                            ls0 += p0;
+                            ls1 += p1;
+                            lr0 += u2f(pk[i] << 16);
+                            lr1 += u2f(pk[i] & 0xffff0000u);
+                        }
                     }
+                    if (PIPE && h == 0 && jj > 0) {
+                        // P's columns are free once the previous P V has read them
+                        if (!__all_sync(0xffffffffu, mbar_wait(my_o, (cbt + jj - 1) & 1, wd, kSiteSoftO))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    if constexpr (kPC == 16) tmem_st16(tP + h * 16, pk);
+                    else tmem_st32(tP + h * 32, pk);
                 }
-                if (PIPE && h == 0 && jj > 0) {
-                    // P's columns are free once the previous P V has read them
-                    if (!__all_sync(0xffffffffu, mbar_wait(my_o, (jj - 1) & 1, wd, kSiteSoftO))) {
+                if (!ok) break;
+                if constexpr (PAIRED_SUMS) {
+                    const float2 a2 = f2_unpack(ls2), b2 = f2_unpack(lr2);
+                    ls0 = a2.x;
+                    ls1 = a2.y;
+                    lr0 = b2.x;
+                    lr1 = b2.y;
+                }
+                if constexpr (MASK == kMaskNone) {
+                    l = __fadd_rn(l, __fadd_rn(ls0, ls1));
+                    l_mma = __fadd_rn(l_mma, __fadd_rn(lr0, lr1));
+                } else {
+                    l += ls0 + ls1;
+                    l_mma += lr0 + lr1;
+                }
+                if (jj > 0 && __any_sync(0xffffffffu, grow)) {
+                    // rescale this warp's 32 rows of O once P_{j-1} V_{j-1} has landed (done after
+                    // P_j is written so the S registers are dead; P_j V_j waits for p_ready)
+                    if (!__all_sync(0xffffffffu, mbar_wait(my_o, (cbt + jj - 1) & 1, wd, kSiteSoftO))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                }
-                if constexpr (kPC == 16) tmem_st16(tP + h * 16, pk);
-                else tmem_st32(tP + h * 32, pk);
-            }
-            if (!ok) break;
-            if constexpr (PAIRED_SUMS) {
-                const float2 a2 = f2_unpack(ls2), b2 = f2_unpack(lr2);
-                ls0 = a2.x;
-                ls1 = a2.y;
-                lr0 = b2.x;
-                lr1 = b2.y;
-            }
-            if constexpr (MASK == kMaskNone) {
-                l = __fadd_rn(l, __fadd_rn(ls0, ls1));
-                l_mma = __fadd_rn(l_mma, __fadd_rn(lr0, lr1));
-            } else {
-                l += ls0 + ls1;
-                l_mma += lr0 + lr1;
-            }
-            if (jj > 0 && __any_sync(0xffffffffu, grow)) {
-                // rescale this warp's 32 rows of O once P_{j-1} V_{j-1} has landed (done after
-                // P_j is written so the S registers are dead; P_j V_j waits for p_ready)
-                if (!__all_sync(0xffffffffu, mbar_wait(my_o, (jj - 1) & 1, wd, kSiteSoftO))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c0, o);
-                    tmem_ld_wait(o);
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c0, o);
+                        tmem_ld_wait(o);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
-                    tmem_st32(tO + c0, o);
+                        for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+                        tmem_st32(tO + c0, o);
+                    }
                 }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(my_p);
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(my_p);
-        }
 
-        // --------------------------------------------------------- epilogue --
-        bool epi = ok && nbt > 0;
-        if (epi) epi = __all_sync(0xffffffffu, mbar_wait(my_o, (nbt - 1) & 1, wd, kSiteEpi));
-        if (epi) {
-            tc_fence_after();
-            const float inv_l = 1.f / l_mma;
-            const int64_t bh_row = static_cast<int64_t>(bh) * N + row;
-            if (O32) {
-                float* dst = p.O32 + bh_row * D;
+            // --------------------------------------------------------- epilogue --
+            bool epi = ok && nbt > 0;
+            if (epi) epi = __all_sync(0xffffffffu, mbar_wait(my_o, (cbt + nbt - 1) & 1, wd, kSiteEpi));
+            cbt += nbt;
+            if constexpr (PERSIST) {
+                // O / l in bf16, 64 columns (one TMA box) at a time, through this tile's
+                // staging area to a TMA store; O's columns go to the next item's P V
+                // once both halves are read (one o_free phase per item, also for an
+                // empty tile).  Thread 0 of the warpgroup issues the stores and waits
+                // for a store's read of the area before the area is written again.
+                const float inv_l = epi ? 1.f / l_mma : 0.f;
+                uint8_t* stage = smem + (t ? L::kOStage1 : L::kOStage0);
+                if (epi) tc_fence_after();
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c0, o);
-                    tmem_ld_wait(o);
-                    if (row < N) {
+                for (int h = 0; h < D / 64; ++h) {
+                    if (r == 0) bulk_wait_read<0>();  // the area's previous store has read it
+                    named_bar_sync(1 + t, 128);
+                    if (epi) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4*>(dst + c0 + i) =
-                                make_float4(u2f(o[i]) * inv_l, u2f(o[i + 1]) * inv_l,
-                                            u2f(o[i + 2]) * inv_l, u2f(o[i + 3]) * inv_l);
+                        for (int c = 0; c < 2; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(tO + 64 * h + 32 * c, o);
+                            tmem_ld_wait(o);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint4 v;
+                                v.x = pack_bf16(u2f(o[8 * q + 0]) * inv_l, u2f(o[8 * q + 1]) * inv_l);
+                                v.y = pack_bf16(u2f(o[8 * q + 2]) * inv_l, u2f(o[8 * q + 3]) * inv_l);
+                                v.z = pack_bf16(u2f(o[8 * q + 4]) * inv_l, u2f(o[8 * q + 5]) * inv_l);
+                                v.w = pack_bf16(u2f(o[8 * q + 6]) * inv_l, u2f(o[8 * q + 7]) * inv_l);
+                                const int chunk = 4 * c + q;
+                                *reinterpret_cast<uint4*>(stage + r * 128 + ((chunk ^ (r & 7)) << 4)) = v;
+                            }
+                        }
+                        fence_async_shared();
+                    }
+                    if (h == D / 64 - 1) {
+                        if (epi) tc_fence_before();
+                        mbar_arrive(bar_of + 8 * t);
+                    }
+                    named_bar_sync(1 + t, 128);
+                    if (r == 0 && epi) {
+                        tma_store_3d(&tmO, smem_addr(stage), 64 * h, q_start, ibh);
+                        bulk_commit();
                     }
                 }
-            } else {
-                uint8_t* stage = smem + (t ? L::kQ1 : L::kQ0);
-#pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + c0, o);
-                    tmem_ld_wait(o);
-                    const int box = c0 / 64;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int chunk = (c0 % 64) / 8 + q;
-                        uint4 v;
-                        v.x = pack_bf16(u2f(o[8 * q + 0]) * inv_l, u2f(o[8 * q + 1]) * inv_l);
-                        v.y = pack_bf16(u2f(o[8 * q + 2]) * inv_l, u2f(o[8 * q + 3]) * inv_l);
-                        v.z = pack_bf16(u2f(o[8 * q + 4]) * inv_l, u2f(o[8 * q + 5]) * inv_l);
-                        v.w = pack_bf16(u2f(o[8 * q + 6]) * inv_l, u2f(o[8 * q + 7]) * inv_l);
-                        *reinterpret_cast<uint4*>(stage + box * L::kBoxBytes + r * 128 +
-                                                  ((chunk ^ (r & 7)) << 4)) = v;
-                    }
-                }
-                fence_async_shared();
+                if (epi && row < N) p.LSE[static_cast<int64_t>(ibh) * N + row] = (m_used + __log2f(l)) * kLn2;
+                continue;
             }
-            if (row < N) p.LSE[bh_row] = (m_used + __log2f(l)) * kLn2;
-        }
-        bool empty_tile = false;
-        if constexpr (SPARSE) {
-            // a tile whose mask row visits no key block: every row is the empty
-            // sum, O = 0 and LSE = -inf, staged as zeros over its Q buffer (the one-tile
-            // kernel loaded Q all the same: that copy must land first)
-            empty_tile = nbt == 0 && q_start < N;
-            if (empty_tile) {
-                bool q_in = true;
-                if constexpr (TILES == 1) q_in = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteEpi));
-                if (q_in) {
+            if (epi) {
+                tc_fence_after();
+                const float inv_l = 1.f / l_mma;
+                const int64_t bh_row = static_cast<int64_t>(ibh) * N + row;
+                if (O32) {
+                    float* dst = p.O32 + bh_row * D;
+#pragma unroll
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c0, o);
+                        tmem_ld_wait(o);
+                        if (row < N) {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4)
+                                *reinterpret_cast<float4*>(dst + c0 + i) =
+                                    make_float4(u2f(o[i]) * inv_l, u2f(o[i + 1]) * inv_l,
+                                                u2f(o[i + 2]) * inv_l, u2f(o[i + 3]) * inv_l);
+                        }
+                    }
+                } else {
                     uint8_t* stage = smem + (t ? L::kQ1 : L::kQ0);
 #pragma unroll
-                    for (int b = 0; b < L::kBoxes; ++b)
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + c0, o);
+                        tmem_ld_wait(o);
+                        const int box = c0 / 64;
 #pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            *reinterpret_cast<uint4*>(stage + b * L::kBoxBytes + r * 128 + c * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
+                        for (int q = 0; q < 4; ++q) {
+                            const int chunk = (c0 % 64) / 8 + q;
+                            uint4 v;
+                            v.x = pack_bf16(u2f(o[8 * q + 0]) * inv_l, u2f(o[8 * q + 1]) * inv_l);
+                            v.y = pack_bf16(u2f(o[8 * q + 2]) * inv_l, u2f(o[8 * q + 3]) * inv_l);
+                            v.z = pack_bf16(u2f(o[8 * q + 4]) * inv_l, u2f(o[8 * q + 5]) * inv_l);
+                            v.w = pack_bf16(u2f(o[8 * q + 6]) * inv_l, u2f(o[8 * q + 7]) * inv_l);
+                            *reinterpret_cast<uint4*>(stage + box * L::kBoxBytes + r * 128 +
+                                                      ((chunk ^ (r & 7)) << 4)) = v;
+                        }
+                    }
                     fence_async_shared();
-                    if (row < N) p.LSE[static_cast<int64_t>(bh) * N + row] = -INFINITY;
                 }
-                epi = q_in;
+                if (row < N) p.LSE[bh_row] = (m_used + __log2f(l)) * kLn2;
             }
-        }
-        if (!O32 && (nbt > 0 || empty_tile)) {
-            // every thread of the warpgroup reaches this barrier, even after an abort
-            named_bar_sync(1 + t, 128);
-            if (r == 0 && epi) {
-                const uint32_t src = sbase + (t ? L::kQ1 : L::kQ0);
-                for (int b = 0; b < L::kBoxes; ++b)
-                    tma_store_3d(&tmO, src + b * L::kBoxBytes, b * 64, q_start, bh);
-                bulk_commit();
-                bulk_wait_read<0>();
+            bool empty_tile = false;
+            if constexpr (SPARSE) {
+                // a tile whose mask row visits no key block: every row is the empty
+                // sum, O = 0 and LSE = -inf, staged as zeros over its Q buffer (the one-tile
+                // kernel loaded Q all the same: that copy must land first)
+                empty_tile = nbt == 0 && q_start < N;
+                if (empty_tile) {
+                    bool q_in = true;
+                    if constexpr (TILES == 1) q_in = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteEpi));
+                    if (q_in) {
+                        uint8_t* stage = smem + (t ? L::kQ1 : L::kQ0);
+#pragma unroll
+                        for (int b = 0; b < L::kBoxes; ++b)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c)
+                                *reinterpret_cast<uint4*>(stage + b * L::kBoxBytes + r * 128 + c * 16) =
+                                    make_uint4(0u, 0u, 0u, 0u);
+                        fence_async_shared();
+                        if (row < N) p.LSE[static_cast<int64_t>(ibh) * N + row] = -INFINITY;
+                    }
+                    epi = q_in;
+                }
+            }
+            if (!O32 && (nbt > 0 || empty_tile)) {
+                // every thread of the warpgroup reaches this barrier, even after an abort
+                named_bar_sync(1 + t, 128);
+                if (r == 0 && epi) {
+                    const uint32_t src = sbase + (t ? L::kQ1 : L::kQ0);
+                    for (int b = 0; b < L::kBoxes; ++b)
+                        tma_store_3d(&tmO, src + b * L::kBoxBytes, b * 64, q_start, ibh);
+                    bulk_commit();
+                    bulk_wait_read<0>();
+                }
             }
         }
     }
 
     // ------------------------------------------------------------ teardown --
+    if (PERSIST && warp < 4 * TILES && (threadIdx.x & 127) == 0) bulk_wait_read<0>();
     if (sh.abort_flag) drain_after_abort();
     tc_fence_before();
     __syncthreads();
@@ -836,23 +1005,48 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     } else if (!make_tile_map(&to, a.O, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.BH, 64, kBM)) {
         return cudaErrorInvalidValue;
     }
+    // d = 128 sliding-window pairs (bf16 O) with more pairs than SMs: the
+    // persistent kernel, so that one item's epilogue and the next item's first
+    // loads overlap the work of the SM's other tile.  (Without a mask it measured
+    // 1-4% slower than one CTA per pair: the hardware's dynamic CTA scheduling
+    // balances the causal pairs better than a static list, and the per-item
+    // loop costs the softmax some registers.)
+    constexpr bool kCanPersist = D == 128 && TILES == 2 && !O32 && MASK == kMaskWindow;
+    const int n_pairs = (a.N + TILES * kBM - 1) / (TILES * kBM);
+    const long long items = static_cast<long long>(a.BH) * n_pairs;
+    int sms = 0;
+    if (kCanPersist) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cudaGetLastError();
+    }
+    if (items > (1ll << 30)) return cudaErrorInvalidValue;
+    const bool persist = kCanPersist && items > sms;
     constexpr auto kern = &fa_fwd_kernel<D, CAUSAL, O32, MASK, TILES>;
-    cudaError_t e = set_max_dyn_smem_once<kern>(L::kDynSmem);
+    constexpr auto kern_p = &fa_fwd_kernel<D, CAUSAL, O32, MASK, TILES, kCanPersist>;
+    cudaError_t e = persist ? set_max_dyn_smem_once<kern_p>(L::kDynSmemPersist)
+                            : set_max_dyn_smem_once<kern>(L::kDynSmem);
     if (e != cudaSuccess) return e;
     FwdParams p;
     p.LSE = a.LSE;
     p.O32 = O32 ? static_cast<float*>(a.O) : nullptr;
+    p.O16 = O32 ? nullptr : static_cast<__nv_bfloat16*>(a.O);
+    p.BH = a.BH;
+    p.items = static_cast<int>(items);
     p.N = a.N;
     p.window = (a.window > 0 && a.window < a.N) ? a.window : 0;
     p.blocks = a.blocks;
     p.blocks_head_stride = a.blocks_head_stride;
-    p.n_pairs = (a.N + TILES * kBM - 1) / (TILES * kBM);
+    p.n_pairs = n_pairs;
     p.scale_log2 = a.tau * kLog2e;
     p.err = a.err;
     p.wait_limit_ns = a.wait_limit_ns;
     dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(p.n_pairs));
+    if (persist) grid = dim3(static_cast<unsigned>(sms));
     if (a.ev_start) cudaEventRecord(a.ev_start, stream);
-    kern<<<grid, threads_for(TILES), L::kDynSmem, stream>>>(tq, tk, tv, to, p);
+    if (persist) kern_p<<<grid, threads_for(TILES), L::kDynSmemPersist, stream>>>(tq, tk, tv, to, p);
+    else kern<<<grid, threads_for(TILES), L::kDynSmem, stream>>>(tq, tk, tv, to, p);
     e = cudaGetLastError();
     if (e == cudaSuccess && a.ev_stop) e = cudaEventRecord(a.ev_stop, stream);
     return e;

@@ -82,6 +82,36 @@ def test_ragged_lengths(N, d, causal):
     check_lse(lse, l_ref)
 
 
+# d = 128 problems with more (batch*head, tile pair) items than SMs, ragged,
+# and with an odd number of query tiles, so the last pair of each head has an
+# empty second tile.
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,N", [(1, 40, 1100), (2, 48, 520), (1, 160, 256)])
+def test_many_pairs_forward_parity(B, H, N, causal):
+    x = draw(B, H, N, 128, seed=900 + N + H, with_do=False)
+    tau = 1 / math.sqrt(128)
+    o_ref, l_ref = oracle.fwd(x["q"], x["k"], x["v"], tau, causal)
+    o, lse = gpu_fwd(x, causal, tau)
+    check_o(o, o_ref)
+    check_lse(lse, l_ref)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_matches_per_head_runs(causal):
+    """A head's O and LSE do not depend on how many heads share the launch: a
+    48-head run (240 pairs) equals, bitwise, one-head runs, and the fp32-O
+    kernel's LSE equals the bf16 one's."""
+    B, H, N, d = 1, 48, 1200, 128
+    x = draw(B, H, N, d, seed=91, with_do=False)
+    o, lse = gpu_fwd(x, causal, 0.1)
+    _, lse32 = gpu_fwd(x, causal, 0.1, o32=True)
+    assert torch.equal(lse32, lse)
+    for h in (0, 23, 47):
+        xh = {n: x[n][:, h:h + 1].contiguous() for n in ("q", "k", "v")}
+        ho, hl = gpu_fwd(xh, causal, 0.1)
+        assert torch.equal(o[:, h:h + 1], ho) and torch.equal(lse[:, h:h + 1], hl)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_non_default_tau(causal):
     x = draw(1, 2, 300, 64, seed=7, with_do=False)

@@ -49,6 +49,24 @@ def test_window_matches_oracle(N, w, d):
     check_grad(dv, rv, "dV")
 
 
+# d = 128 windows with more (batch*head, tile pair) items than SMs run the
+# persistent forward (one CTA per SM walking a list of pairs): parity on a
+# ragged shape with an empty second tile in each head's last pair, and one-head
+# runs (the one-CTA-per-pair kernel) equal bitwise.
+def test_persistent_window_forward():
+    B, H, N, d, w = 1, 64, 1100, 128, 300
+    x = draw(B, H, N, d, seed=93, with_do=False)
+    tau = 1 / math.sqrt(d)
+    o, lse, _ = gpu(x, tau, w, backward=False)
+    o_ref, l_ref = oracle.fwd(x["q"], x["k"], x["v"], tau, True, window=w)
+    check_o(o, o_ref)
+    check_lse(lse, l_ref)
+    for h in (0, 63):
+        xh = {n: x[n][:, h:h + 1].contiguous() for n in ("q", "k", "v")}
+        ho, hl, _ = gpu(xh, tau, w, backward=False)
+        assert torch.equal(o[:, h:h + 1], ho) and torch.equal(lse[:, h:h + 1], hl)
+
+
 def test_window_one_returns_own_value_bitwise():
     x = draw(1, 3, 700, 128, seed=7)
     o, _, _ = gpu(x, 1 / math.sqrt(128), 1, backward=False)
