@@ -29,12 +29,12 @@
 //   - causal: key blocks wholly above the diagonal are never loaded; the
 //     diagonal block is masked element-wise.  Keys >= N in a ragged last
 //     block are masked the same way;
-//   - d = 128 sliding windows run persistently when there are more tile pairs
-//     than SMs (PERSIST below): one CTA per SM walks a list of (batch*head,
-//     pair) items and keeps its barriers, tensor memory and K/V ring; the next
-//     item's Q tiles and first K/V blocks load while the current item's
-//     epilogue runs, and O is staged in a buffer of its own, so an item change
-//     costs only the epilogue.
+//   - d = 128 sliding windows and d = 64 without a mask run persistently when
+//     there are more tile pairs than SMs (PERSIST below): one CTA per SM walks
+//     a list of (batch*head, pair) items and keeps its barriers, tensor memory
+//     and K/V ring; the next item's Q tiles and first K/V blocks load while the
+//     current item's epilogue runs, and O is staged in a buffer of its own, so
+//     an item change costs only the epilogue.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -74,8 +74,8 @@ struct FwdLayout {
     static constexpr int kBytes = kRing + kStages * kTileBytes;
     static constexpr int kDynSmem = kBytes + 1024;  // + alignment slack
     // persistent kernel: O of tile t is staged 64 columns (one TMA box) at a time in
-    // a 16 KB area of its own, since Q_t is already loading the next item's tile
-    static constexpr int kOStage0 = kBytes, kOStage1 = kBytes + kBoxBytes;
+    // a 16 KB area of its own at kBytes + t kBoxBytes, since Q_t is already loading
+    // the next item's tile
     static constexpr int kDynSmemPersist = kBytes + 2 * kBoxBytes + 1024;
     static constexpr uint32_t kTmemS0 = 0, kTmemS1 = TILES == 2 ? 128 : 0;
     static constexpr uint32_t kTmemO0 = TILES == 2 ? 256 : 128, kTmemO1 = TILES == 2 ? 256 + D : 128;
@@ -180,8 +180,8 @@ __device__ __forceinline__ FwdItem fwd_item(int bh, int pair, int N, int n_kv, i
 
 // MASK: kMaskNone; kMaskWindow, a causal sliding window of p.window keys (only
 // with CAUSAL); kMaskBlocks, the block mask p.blocks (bf16 O only).  PERSIST:
-// one CTA per SM walks a list of (batch*head, pair) items (d = 128, two tiles,
-// bf16 O, no block mask).
+// one CTA per SM walks a list of (batch*head, pair) items (d = 128 sliding
+// windows or d = 64 without a mask, bf16 O).
 template <int D, bool CAUSAL, bool O32, int MASK, int TILES, bool PERSIST = false>
 __global__ void __launch_bounds__(threads_for(TILES), TILES == 2 ? 1 : 2)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -195,8 +195,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // j + 1 is issued as soon as the softmax has read S of block j, and the
     // softmax runs from block to block without waiting for P V and the next S
     constexpr bool PIPE = D == 64 && MASK == kMaskNone;
-    static_assert(!PERSIST || (D == 128 && TILES == 2 && !O32 && !SPARSE),
-                  "persistent: d = 128 pairs, bf16 O");
+    static_assert(!PERSIST || (TILES == 2 && !O32 && ((D == 128 && LOCAL) || (D == 64 && PIPE))),
+                  "persistent: d = 128 sliding-window pairs or d = 64 pairs, bf16 O");
     // the row sums as paired fp32 adds (bitwise the same sums): measured faster
     // in the one-tile kernel, slower in the two-tile one (register pressure),
     // except at d = 128 with a bf16 O (the sliding-window kernel too: 5% faster,
@@ -480,56 +480,80 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         }
                     }
                 } else if constexpr (PIPE) {
-                    // iteration j issues S(j) of both tiles (each once the softmax has
-                    // read S(j - 1)), then P(j - 1) V(j - 1) of both tiles
-                    const int hi[2] = {hi0, n_blk1 > 0 ? hi1 : 0};
+                    // iteration j issues S(j) of both tiles (each once the softmax has read
+                    // the tile's previous S), then P(j - 1) V(j - 1) of both tiles.  Ring
+                    // loads (g0), each tile's blocks (cb) and Q fills (k) are counted
+                    // across the items; the barrier phases follow them.
                     const uint32_t tP[2] = {tmem + L::kTmemP0, tmem + L::kTmemP1};
-                    bool ok = __all_sync(0xffffffffu, mbar_wait(bar_q, 0, wd, kSiteMmaQ));
-                    for (int j = 0; ok && j <= nb; ++j) {
-                        if (j < nb) {
-                            const int lk = j == 0 ? 0 : 2 * j - 1, sk = lk % L::kStages;  // K_j
-                            if (!__all_sync(0xffffffffu, mbar_wait(bar_kv_full + 8 * sk,
-                                                                   (lk / L::kStages) & 1, wd, kSiteMmaKV))) {
-                                ok = false;
-                                break;
-                            }
+                    bool ok = true;
+                    int g0 = 0;            // ring loads of the earlier items
+                    int cb0 = 0, cb1 = 0;  // blocks of tile 0 / 1 in the earlier items
+                    FwdItem it;
+                    for (int k = 0; (PERSIST || k == 0) && ok && item_at(k, it); ++k) {
+                        const int hi[2] = {it.hi0, it.n_blk1 > 0 ? it.hi1 : 0};
+                        const int cb[2] = {cb0, cb1};
+                        const int nbk = it.nb;
+                        ok = __all_sync(0xffffffffu, mbar_wait(bar_q, k & 1, wd, kSiteMmaQ));
+                        for (int j = 0; ok && j <= nbk; ++j) {
+                            if (j < nbk) {
+                                const int lk = g0 + (j == 0 ? 0 : 2 * j - 1), sk = lk % L::kStages;  // K_j
+                                if (!__all_sync(0xffffffffu, mbar_wait(bar_kv_full + 8 * sk,
+                                                                       (lk / L::kStages) & 1, wd, kSiteMmaKV))) {
+                                    ok = false;
+                                    break;
+                                }
 #pragma unroll
-                            for (int t = 0; t < TILES; ++t) {
-                                if (ok && j < hi[t]) {
-                                    if (j > 0)
-                                        ok = __all_sync(0xffffffffu, mbar_wait(bar_sf + 8 * t, (j - 1) & 1, wd,
-                                                                               kSiteMmaP));
-                                    if (ok) {
-                                        tc_fence_after();
-                                        issue_s<D>(tS[t], qlo[t], klo0 + sk * kSlot);
-                                        mma_commit_warp(bar_s + 8 * t);
+                                for (int t = 0; t < TILES; ++t) {
+                                    if (ok && j < hi[t]) {
+                                        // the tile's previous S (at j = 0 the previous item's last)
+                                        if (cb[t] + j > 0)
+                                            ok = __all_sync(0xffffffffu, mbar_wait(bar_sf + 8 * t, (cb[t] + j - 1) & 1,
+                                                                                   wd, kSiteMmaP));
+                                        if (ok) {
+                                            tc_fence_after();
+                                            issue_s<D>(tS[t], qlo[t], klo0 + sk * kSlot);
+                                            mma_commit_warp(bar_s + 8 * t);
+                                        }
                                     }
                                 }
+                                if (!ok) break;
+                                mma_commit_warp(bar_kv_empty + 8 * sk);
                             }
-                            if (!ok) break;
-                            mma_commit_warp(bar_kv_empty + 8 * sk);
-                        }
-                        if (j > 0) {
-                            const int lv = min(2 * j, 2 * nb - 1), sv = lv % L::kStages;  // V_(j-1)
-                            if (!__all_sync(0xffffffffu, mbar_wait(bar_kv_full + 8 * sv,
-                                                                   (lv / L::kStages) & 1, wd, kSiteMmaKV))) {
-                                ok = false;
-                                break;
-                            }
+                            if (j > 0) {
+                                const int lv = g0 + min(2 * j, 2 * nbk - 1), sv = lv % L::kStages;  // V_(j-1)
+                                if (!__all_sync(0xffffffffu, mbar_wait(bar_kv_full + 8 * sv,
+                                                                       (lv / L::kStages) & 1, wd, kSiteMmaKV))) {
+                                    ok = false;
+                                    break;
+                                }
 #pragma unroll
-                            for (int t = 0; t < TILES; ++t) {
-                                if (ok && j - 1 < hi[t]) {
-                                    ok = __all_sync(0xffffffffu, mbar_wait(bar_p + 8 * t, (j - 1) & 1, wd, kSiteMmaP));
-                                    if (ok) {
-                                        tc_fence_after();
-                                        issue_pv<D>(tO[t], tP[t], vlo0 + sv * kSlot, j > 1);
-                                        mma_commit_warp(bar_o + 8 * t);
+                                for (int t = 0; t < TILES; ++t) {
+                                    if (ok && j - 1 < hi[t]) {
+                                        // the item's first P V overwrites O: the softmax warps must
+                                        // have read the previous item's O out
+                                        if (PERSIST && j == 1 && k > 0) {
+                                            ok = __all_sync(0xffffffffu,
+                                                            mbar_wait(bar_of + 8 * t, (k - 1) & 1, wd, kSiteMmaOF));
+                                        }
+                                        if (ok)
+                                            ok = __all_sync(0xffffffffu, mbar_wait(bar_p + 8 * t, (cb[t] + j - 1) & 1,
+                                                                                   wd, kSiteMmaP));
+                                        if (ok) {
+                                            tc_fence_after();
+                                            issue_pv<D>(tO[t], tP[t], vlo0 + sv * kSlot, j > 1);
+                                            mma_commit_warp(bar_o + 8 * t);
+                                        }
                                     }
                                 }
+                                if (!ok) break;
+                                mma_commit_warp(bar_kv_empty + 8 * sv);
                             }
-                            if (!ok) break;
-                            mma_commit_warp(bar_kv_empty + 8 * sv);
                         }
+                        // the Q tiles take the next item's once this item's MMAs are done
+                        if (PERSIST && ok) mma_commit_warp(bar_qe);
+                        g0 += 2 * nbk;
+                        cb0 += it.n_blk0;
+                        cb1 += it.n_blk1;
                     }
                 } else {
                     // Ring loads (g), S_t / P_t / P_t V products (cb[t]) and Q fills
@@ -566,11 +590,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                             return w;
                         };
                         if constexpr (!LOCAL) {
-                            // every tile starts at key block 0: tile t takes blocks [0, hi[t]).
-                            // Both tiles' O must be free before the first P V (tile 1's
-                            // epilogue ends about a block after tile 0's, while tile 0 runs
-                            // its first softmax): the block loop stays that of one item.
-                            if (ok) ok = o_free_wait(0) && (hi[1] == 0 || o_free_wait(1));
+                            // every tile starts at key block 0: tile t takes blocks [0, hi[t])
                             for (int j = 0; ok && j < it.nb; ++j) {
                                 const int lv = g0 + 2 * j + 1, lk = g0 + 2 * j + 2;
                                 const int sv = lv % L::kStages, sk = lk % L::kStages;
@@ -863,7 +883,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 // empty tile).  Thread 0 of the warpgroup issues the stores and waits
                 // for a store's read of the area before the area is written again.
                 const float inv_l = epi ? 1.f / l_mma : 0.f;
-                uint8_t* stage = smem + (t ? L::kOStage1 : L::kOStage0);
+                uint8_t* stage = smem + L::kBytes + (t ? L::kBoxBytes : 0);
                 if (epi) tc_fence_after();
 #pragma unroll
                 for (int h = 0; h < D / 64; ++h) {
@@ -1005,13 +1025,17 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     } else if (!make_tile_map(&to, a.O, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.BH, 64, kBM)) {
         return cudaErrorInvalidValue;
     }
-    // d = 128 sliding-window pairs (bf16 O) with more pairs than SMs: the
-    // persistent kernel, so that one item's epilogue and the next item's first
-    // loads overlap the work of the SM's other tile.  (Without a mask it measured
-    // 1-4% slower than one CTA per pair: the hardware's dynamic CTA scheduling
-    // balances the causal pairs better than a static list, and the per-item
-    // loop costs the softmax some registers.)
-    constexpr bool kCanPersist = D == 128 && TILES == 2 && !O32 && MASK == kMaskWindow;
+    // d = 128 sliding-window pairs and d = 64 pairs without a mask (bf16 O), with
+    // more pairs than SMs: the persistent kernel, so that one item's epilogue and
+    // the next item's first loads overlap the work of the SM's other tile
+    // (d = 64: 3-6% faster from 3k to 32k tokens; up to 2k tokens the one-tile
+    // persistent kernel of fa_fwd_short.cu is faster still).  The same form for
+    // d = 128 without a mask measured 1-4% slower than one CTA per pair: the
+    // hardware's dynamic CTA scheduling balances the causal pairs better than a
+    // static list, and the per-item loop cost the softmax more than the fixed
+    // costs it saved.
+    constexpr bool kCanPersist =
+        TILES == 2 && !O32 && ((D == 128 && MASK == kMaskWindow) || (D == 64 && MASK == kMaskNone));
     const int n_pairs = (a.N + TILES * kBM - 1) / (TILES * kBM);
     const long long items = static_cast<long long>(a.BH) * n_pairs;
     int sms = 0;

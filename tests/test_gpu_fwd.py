@@ -82,14 +82,16 @@ def test_ragged_lengths(N, d, causal):
     check_lse(lse, l_ref)
 
 
-# d = 128 problems with more (batch*head, tile pair) items than SMs, ragged,
-# and with an odd number of query tiles, so the last pair of each head has an
-# empty second tile.
+# Problems with more (batch*head, tile pair) items than SMs, ragged, and with
+# an odd number of query tiles, so the last pair of each head has an empty
+# second tile.  At d = 64 beyond 2048 tokens these run the persistent two-tile
+# forward (one CTA per SM walking the pairs).
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("B,H,N", [(1, 40, 1100), (2, 48, 520), (1, 160, 256)])
-def test_many_pairs_forward_parity(B, H, N, causal):
-    x = draw(B, H, N, 128, seed=900 + N + H, with_do=False)
-    tau = 1 / math.sqrt(128)
+@pytest.mark.parametrize("B,H,N,d", [(1, 40, 1100, 128), (2, 48, 520, 128), (1, 160, 256, 128),
+                                     (1, 40, 2100, 64), (2, 24, 2200, 64)])
+def test_many_pairs_forward_parity(B, H, N, d, causal):
+    x = draw(B, H, N, d, seed=900 + N + H, with_do=False)
+    tau = 1 / math.sqrt(d)
     o_ref, l_ref = oracle.fwd(x["q"], x["k"], x["v"], tau, causal)
     o, lse = gpu_fwd(x, causal, tau)
     check_o(o, o_ref)
@@ -97,11 +99,13 @@ def test_many_pairs_forward_parity(B, H, N, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_forward_matches_per_head_runs(causal):
-    """A head's O and LSE do not depend on how many heads share the launch: a
-    48-head run (240 pairs) equals, bitwise, one-head runs, and the fp32-O
-    kernel's LSE equals the bf16 one's."""
-    B, H, N, d = 1, 48, 1200, 128
+@pytest.mark.parametrize("N,d", [(1200, 128), (2300, 64)])
+def test_forward_matches_per_head_runs(causal, N, d):
+    """A head's O and LSE do not depend on how many heads share the launch (at
+    d = 64 and 2300 tokens: the persistent kernel against one-head runs of the
+    one-CTA-per-pair kernel): a 48-head run equals, bitwise, one-head runs, and
+    the fp32-O kernel's LSE equals the bf16 one's."""
+    B, H = 1, 48
     x = draw(B, H, N, d, seed=91, with_do=False)
     o, lse = gpu_fwd(x, causal, 0.1)
     _, lse32 = gpu_fwd(x, causal, 0.1, o32=True)
