@@ -198,10 +198,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     static_assert(!PERSIST || (TILES == 2 && !O32 && ((D == 128 && LOCAL) || (D == 64 && PIPE))),
                   "persistent: d = 128 sliding-window pairs or d = 64 pairs, bf16 O");
     // the row sums as paired fp32 adds (bitwise the same sums): measured faster
-    // in the one-tile kernel, slower in the two-tile one (register pressure),
-    // except at d = 128 with a bf16 O (the sliding-window kernel too: 5% faster,
-    // and its spills are gone)
-    constexpr bool PAIRED_SUMS = (PIPE && TILES == 1) || (D == 128 && MASK != kMaskBlocks && !O32);
+    // with a bf16 O at d = 128 (the sliding-window kernel too: 5% faster, and its
+    // spills are gone) and in the d = 64 pipelined kernels (two-tile: 2-3%)
+    constexpr bool PAIRED_SUMS = (PIPE && !O32) || (D == 128 && MASK != kMaskBlocks && !O32);
     // P is converted and stored in chunks of kPC packed columns: 16 at d = 128, which
     // frees the registers the paired sums need there, 32 at d = 64 and for the fp32
     // O (measured faster, and without spills, there)
