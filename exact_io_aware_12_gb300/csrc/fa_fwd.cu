@@ -801,7 +801,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 // the scale-and-subtract runs as one paired fp32 FMA per two scores
                 const uint64_t c2 = f2_pack(sl2, sl2), nm2 = f2_pack(neg_m, neg_m);
                 float ls0 = 0.f, ls1 = 0.f, lr0 = 0.f, lr1 = 0.f;
-                uint64_t ls2 = 0, lr2 = 0;  // PAIRED_SUMS: the same sums, paired (bitwise equal)
+                uint64_t ls2 = 0;  // PAIRED_SUMS: ls0 and ls1 as one pair (bitwise the same sums)
 #pragma unroll
                 for (int h = 0; h < 64 / kPC; ++h) {
                     uint32_t pk[kPC];
@@ -814,13 +814,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         pk[i] = pack_bf16(p0, p1);
                         if constexpr (PAIRED_SUMS) {
                             ls2 = fadd2(ls2, f2_pack(p0, p1));
-                            lr2 = fadd2(lr2, f2_pack(u2f(pk[i] << 16), u2f(pk[i] & 0xffff0000u)));
                         } else {
                             ls0 += p0;
                             ls1 += p1;
-                            lr0 += u2f(pk[i] << 16);
-                            lr1 += u2f(pk[i] & 0xffff0000u);
                         }
+                        // the bf16 values straight from the packed pair (16k causal:
+                        // 0.725 -> 0.700 ms against unpacking them for fp32 adds)
+                        add_bf16x2_f32(pk[i], lr0, lr1);
                     }
                     if (PIPE && h == 0 && jj > 0) {
                         // P's columns are free once the previous P V has read them
@@ -835,11 +835,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                 }
                 if (!ok) break;
                 if constexpr (PAIRED_SUMS) {
-                    const float2 a2 = f2_unpack(ls2), b2 = f2_unpack(lr2);
+                    const float2 a2 = f2_unpack(ls2);
                     ls0 = a2.x;
                     ls1 = a2.y;
-                    lr0 = b2.x;
-                    lr1 = b2.y;
                 }
                 if constexpr (MASK == kMaskNone) {
                     l = __fadd_rn(l, __fadd_rn(ls0, ls1));

@@ -307,7 +307,8 @@ fa_fwd_short_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                 // l_mma sums the bf16 P values the P V MMA consumes (it normalises
                 // O), l the fp32 values (it gives LSE); paired fp32 adds
                 const uint64_t c2 = f2_pack(sl2, sl2), nm2 = f2_pack(neg_m, neg_m);
-                uint64_t ls2 = 0, lr2 = 0;
+                uint64_t ls2 = 0;
+                float lr0 = 0.f, lr1 = 0.f;  // the bf16 sums, added straight from the packed pairs
 #pragma unroll
                 for (int h = 0; h < 64 / kPC; ++h) {
                     uint32_t pk[kPC];
@@ -319,7 +320,7 @@ fa_fwd_short_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                         const float p0 = ex2(x.x), p1 = ex2(x.y);
                         pk[i] = pack_bf16(p0, p1);
                         ls2 = fadd2(ls2, f2_pack(p0, p1));
-                        lr2 = fadd2(lr2, f2_pack(u2f(pk[i] << 16), u2f(pk[i] & 0xffff0000u)));
+                        add_bf16x2_f32(pk[i], lr0, lr1);
                     }
                     if (h == 0 && g > 0) {
                         // P's columns are free once the previous P V (of this or the
@@ -333,9 +334,9 @@ fa_fwd_short_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_consta
                     tmem_st32(tP + h * 32, pk);
                 }
                 if (!ok) break;
-                const float2 a2 = f2_unpack(ls2), b2 = f2_unpack(lr2);
+                const float2 a2 = f2_unpack(ls2);
                 l = __fadd_rn(l, __fadd_rn(a2.x, a2.y));
-                l_mma = __fadd_rn(l_mma, __fadd_rn(b2.x, b2.y));
+                l_mma = __fadd_rn(l_mma, __fadd_rn(lr0, lr1));
                 if (jj > 0 && __any_sync(0xffffffffu, grow)) {
                     // rescale this warp's rows of O once the previous P V has landed
                     if (!__all_sync(0xffffffffu, mbar_wait(bar_o, (g - 1) & 1, wd, kSiteSoftO))) {

@@ -598,6 +598,15 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+// lo += the low bf16 half of x, hi += the high half: each half is widened to
+// fp32 (exactly) and added with one round-to-nearest, so the sums are those of
+// u2f(x << 16) and u2f(x & 0xffff0000) added in fp32, without the unpacking
+// instructions (add.f32.bf16 takes the 16-bit half as it is)
+__device__ __forceinline__ void add_bf16x2_f32(uint32_t x, float& lo, float& hi) {
+    asm("{\n\t.reg .b16 l16, h16;\n\tmov.b32 {l16, h16}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l16, %0;\n\tadd.rn.f32.bf16 %1, h16, %1;\n\t}"
+        : "+f"(lo), "+f"(hi) : "r"(x));
+}
 __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
