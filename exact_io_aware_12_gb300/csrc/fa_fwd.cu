@@ -29,7 +29,8 @@
 //   - causal: key blocks wholly above the diagonal are never loaded; the
 //     diagonal block is masked element-wise.  Keys >= N in a ragged last
 //     block are masked the same way;
-//   - d = 128 sliding windows and d = 64 without a mask run persistently when
+//   - two-tile problems with a bf16 O (d = 128 sliding windows, d = 64 without a
+//     mask, d = 128 without a mask up to 4096 tokens) run persistently when
 //     there are more tile pairs than SMs (PERSIST below): one CTA per SM walks
 //     a list of (batch*head, pair) items and keeps its barriers, tensor memory
 //     and K/V ring; the next item's Q tiles and first K/V blocks load while the
@@ -61,6 +62,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 2^8
 enum : int { kMaskNone = 0, kMaskWindow = 1, kMaskBlocks = 2 };
 constexpr int kMaskWords = kMaxMaskBlocks / 32;
 constexpr int kSingleTileMaxN = 2048;  // d = 64 up to this length: one tile per CTA
+constexpr int kPersistMaxN128 = 4096;  // d = 128 without a mask up to this length: the persistent pairs
 
 template <int D, int TILES = 2>
 struct FwdLayout {
@@ -180,8 +182,8 @@ __device__ __forceinline__ FwdItem fwd_item(int bh, int pair, int N, int n_kv, i
 
 // MASK: kMaskNone; kMaskWindow, a causal sliding window of p.window keys (only
 // with CAUSAL); kMaskBlocks, the block mask p.blocks (bf16 O only).  PERSIST:
-// one CTA per SM walks a list of (batch*head, pair) items (d = 128 sliding
-// windows or d = 64 without a mask, bf16 O).
+// one CTA per SM walks a list of (batch*head, pair) items (two tiles, bf16 O,
+// no block mask).
 template <int D, bool CAUSAL, bool O32, int MASK, int TILES, bool PERSIST = false>
 __global__ void __launch_bounds__(threads_for(TILES), TILES == 2 ? 1 : 2)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -195,8 +197,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // j + 1 is issued as soon as the softmax has read S of block j, and the
     // softmax runs from block to block without waiting for P V and the next S
     constexpr bool PIPE = D == 64 && MASK == kMaskNone;
-    static_assert(!PERSIST || (TILES == 2 && !O32 && ((D == 128 && LOCAL) || (D == 64 && PIPE))),
-                  "persistent: d = 128 sliding-window pairs or d = 64 pairs, bf16 O");
+    static_assert(!PERSIST || (TILES == 2 && !O32 && !SPARSE && (D == 128 || PIPE)),
+                  "persistent: two-tile pairs with a bf16 O, no block mask");
     // the row sums as paired fp32 adds (bitwise the same sums): measured faster
     // with a bf16 O at d = 128 (the sliding-window kernel too: 5% faster, and its
     // spills are gone) and in the d = 64 pipelined kernels (two-tile: 2-3%)
@@ -589,7 +591,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                             return w;
                         };
                         if constexpr (!LOCAL) {
-                            // every tile starts at key block 0: tile t takes blocks [0, hi[t])
+                            // every tile starts at key block 0: tile t takes blocks [0, hi[t]).
+                            // Both tiles' O must be free before the first P V (tile 1's
+                            // epilogue ends about a block after tile 0's, while tile 0 runs
+                            // its first softmax): the block loop stays that of one item.
+                            if (ok) ok = o_free_wait(0) && (hi[1] == 0 || o_free_wait(1));
                             for (int j = 0; ok && j < it.nb; ++j) {
                                 const int lv = g0 + 2 * j + 1, lk = g0 + 2 * j + 2;
                                 const int sv = lv % L::kStages, sk = lk % L::kStages;
@@ -1022,17 +1028,15 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     } else if (!make_tile_map(&to, a.O, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, a.N, a.BH, 64, kBM)) {
         return cudaErrorInvalidValue;
     }
-    // d = 128 sliding-window pairs and d = 64 pairs without a mask (bf16 O), with
-    // more pairs than SMs: the persistent kernel, so that one item's epilogue and
-    // the next item's first loads overlap the work of the SM's other tile
-    // (d = 64: 3-6% faster from 3k to 32k tokens; up to 2k tokens the one-tile
-    // persistent kernel of fa_fwd_short.cu is faster still).  The same form for
-    // d = 128 without a mask measured 1-4% slower than one CTA per pair: the
-    // hardware's dynamic CTA scheduling balances the causal pairs better than a
-    // static list, and the per-item loop cost the softmax more than the fixed
-    // costs it saved.
-    constexpr bool kCanPersist =
-        TILES == 2 && !O32 && ((D == 128 && MASK == kMaskWindow) || (D == 64 && MASK == kMaskNone));
+    // Pairs with a bf16 O and more pairs than SMs: the persistent kernel, so that
+    // one item's epilogue and the next item's first loads overlap the work of the
+    // SM's other tile.  Measured against one CTA per pair: d = 64 3-6% faster from
+    // 3k to 32k tokens (up to 2k tokens the one-tile persistent kernel of
+    // fa_fwd_short.cu is faster still); d = 128 sliding windows 3% faster; d = 128
+    // without a mask 1-7% faster up to 4096 tokens, where the items are short, but
+    // 1-3% slower from 8192 up, where the hardware's dynamic CTA scheduling
+    // balances long causal pairs better than a static list.
+    constexpr bool kCanPersist = TILES == 2 && !O32 && MASK != kMaskBlocks && (D == 128 || MASK == kMaskNone);
     const int n_pairs = (a.N + TILES * kBM - 1) / (TILES * kBM);
     const long long items = static_cast<long long>(a.BH) * n_pairs;
     int sms = 0;
@@ -1043,7 +1047,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
             return cudaGetLastError();
     }
     if (items > (1ll << 30)) return cudaErrorInvalidValue;
-    const bool persist = kCanPersist && items > sms;
+    // d = 128 without a mask: only up to 4096 tokens (below)
+    const bool persist = kCanPersist && items > sms && (D != 128 || MASK != kMaskNone || a.N <= kPersistMaxN128);
     constexpr auto kern = &fa_fwd_kernel<D, CAUSAL, O32, MASK, TILES>;
     constexpr auto kern_p = &fa_fwd_kernel<D, CAUSAL, O32, MASK, TILES, kCanPersist>;
     cudaError_t e = persist ? set_max_dyn_smem_once<kern_p>(L::kDynSmemPersist)
