@@ -63,6 +63,46 @@ enum : int { kMaskNone = 0, kMaskWindow = 1, kMaskBlocks = 2 };
 constexpr int kMaskWords = kMaxMaskBlocks / 32;
 constexpr int kBwdPersistMaxN = 2048;  // d = 64, no mask, up to this length: the persistent kernel
 
+// Block-mask backward: a key tile visited by many query tiles (the global anchors of
+// a local + global mask are visited by every one) sets the kernel's length alone
+// when the rest of the work is short, so its query list is split into chunks that
+// extra CTAs run.  A plan kernel picks the chunks from the mask; each chunk adds
+// its dQ into the accumulator as usual and writes its partial dK, dV (fp32) to a
+// slot, and the last chunk of a tile to finish adds the slots in chunk order (a
+// fixed order: the result does not depend on which chunk finishes last) and writes
+// dK, dV.  The plan and the slots live in the dQ output, which only the dQ
+// conversion kernel writes, afterwards.  Only problems of at most kSplitTilesPerSm
+// key tiles per SM are planned: measured on GB300 (16 heads of 16k tokens, a local
+// + global mask), with more tiles the busiest SM ran within 4% of the mean without
+// a split, and a split that runs the anchors' later query tiles early lost L2 reuse
+// (16% slower), while the plan itself costs about 15 us.
+constexpr int kSplitTilesPerSm = 2;
+constexpr int kSplitMaxChunks = 8;
+constexpr int kSplitMinSteps = 16;     // a chunk of fewer query tiles is not worth a CTA
+constexpr int kSplitCtaSteps = 2;      // a CTA's set-up and epilogue cost about two steps
+constexpr int kPlanThreads = 1024;
+// The plan's arrays in its buffer (byte offsets, each 256-aligned): the number of
+// helper chunks in use (u32); per key tile in launch order kt * BH + bh its chunk
+// count (u8, 1: not split), first partial slot (u32) and finished chunks (u32);
+// per helper CTA its (key tile, chunk) (2 x u32); the planner's query-tile counts
+// per mask head and key tile (u32); then the partial slots, each [dV, dK][128
+// keys][D] fp32.
+struct SplitPlan {
+    size_t hdr, nchunk, slot, help, arrive, cnt, part;
+};
+__host__ __device__ __forceinline__ SplitPlan split_layout(int n_tiles, int n_help) {
+    const auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    SplitPlan s;
+    s.hdr = 0;
+    s.nchunk = 256;
+    s.slot = s.nchunk + up(static_cast<size_t>(n_tiles));
+    s.help = s.slot + up(4 * static_cast<size_t>(n_tiles));
+    s.arrive = s.help + up(8 * static_cast<size_t>(n_help));
+    s.cnt = s.arrive + up(4 * static_cast<size_t>(n_tiles));
+    s.part = s.cnt + up(4 * static_cast<size_t>(n_tiles));
+    return s;
+}
+
 template <int D>
 struct BwdLayout {
     static constexpr int kTile = kBK * D * 2;  // one bf16 [128 x D] tile
@@ -111,6 +151,8 @@ struct BwdBarriers {
     uint64_t dk_done;
     uint32_t tmem_base;
     int abort_flag;
+    int last_chunk;              // split key tile: this CTA's chunk finished last
+    int sp_tile, sp_chunk, sp_nchunk;  // split plan: key tile, chunk, chunks (1: not split)
     uint32_t qbits[kMaskWords];  // kMaskBlocks: bit i = this key tile is visited by query tile i
 };
 
@@ -129,6 +171,9 @@ struct BwdParams {
     int head_group;                 // heads whose key tiles are interleaved in launch order
     int BH;                         // persistent: batch*heads
     int items;                      // persistent: work items (BH key tiles each)
+    uint8_t* plan;                  // block mask: the split plan's buffer (layout: split_layout)
+    int plan_tiles;                 // its key tiles (BH * n_kv), 0: no plan
+    int plan_help;                  // its helper CTAs, launched first
 };
 
 enum : uint32_t {
@@ -198,7 +243,7 @@ __device__ __forceinline__ void mma_mn_mn(uint32_t tmem_d, uint32_t a_lo, uint32
 // MASK: kMaskNone; kMaskWindow, a causal sliding window of p.window keys (only
 // with CAUSAL); kMaskBlocks, the block mask p.blocks.  PERSIST: one CTA per SM
 // walks a list of (key tile, batch*head) work items (no mask).
-template <int D, bool CAUSAL, int MASK, int NWG, bool PERSIST = false>
+template <int D, bool CAUSAL, int MASK, int NWG, bool PERSIST = false, bool SPLIT = false>
 __global__ void __launch_bounds__(bwd_threads(NWG), 1)
 fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -216,6 +261,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     constexpr int kEW = 128 * NWG;      // elementwise threads
     constexpr bool LOCAL = MASK == kMaskWindow;
     constexpr bool SPARSE = MASK == kMaskBlocks;
+    // a block mask with a split plan (its own instance: the plan's code stays out of
+    // the plain block-mask kernel)
+    constexpr bool SPLIT_ = SPARSE && SPLIT;
+    static_assert(!SPLIT || SPARSE, "a split plan needs a block mask");
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
     BwdBarriers& sh = *reinterpret_cast<BwdBarriers*>(smem + L::kBars);
@@ -224,6 +273,26 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // Block mask with a split plan: this CTA's key tile (launch order kt * BH + bh)
+    // and its chunk of the tile's query list.  The first n_help CTAs are helpers,
+    // each running one chunk > 0 of a split tile, or nothing; launched first, the
+    // long tiles' chunks start before the short tiles fill the machine.  The plan
+    // is written by the plan kernel, launched just before: a helper waits for it
+    // here, a key tile's own CTA reads its chunk count later, beside its mask loads.
+    int sp_tile = -1, sp_chunk = 0;
+    if constexpr (SPLIT_) {
+        const int e = static_cast<int>(blockIdx.x);
+        if (e < p.plan_help) {
+            griddep_wait();
+            const SplitPlan pl = split_layout(p.plan_tiles, p.plan_help);
+            if (e >= static_cast<int>(*reinterpret_cast<const uint32_t*>(p.plan + pl.hdr))) return;
+            const uint32_t* help = reinterpret_cast<const uint32_t*>(p.plan + pl.help);
+            sp_tile = static_cast<int>(help[2 * e]);
+            sp_chunk = static_cast<int>(help[2 * e + 1]);
+        } else {
+            sp_tile = e - p.plan_help;
+        }
+    }
     // Work item k of this CTA: (batch*head, key tile), or false past the last.
     // Without PERSIST a CTA has one item, set by its launch position: the launch
     // order (x fastest) walks groups of p.head_group heads; inside a group the key
@@ -244,6 +313,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             return true;
         }
         if (k > 0) return false;
+        if (SPLIT_) {
+            ikv = sp_tile / p.BH;
+            ibh = sp_tile - ikv * p.BH;
+            return true;
+        }
         const long long i = blockIdx.x + static_cast<long long>(gridDim.x) * blockIdx.y;
         const long long per_group = static_cast<long long>(p.head_group) * p.n_kv;
         const int g = static_cast<int>(i / per_group);
@@ -291,6 +365,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
     if (threadIdx.x == 0) {
         sh.abort_flag = 0;
+        if constexpr (SPLIT_) {
+            sh.sp_tile = sp_tile;
+            sh.sp_chunk = sp_chunk;
+        }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_kv + 8 * b, 1);
             mbar_init(bar_kve + 8 * b, 1);
@@ -328,6 +406,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             // bit i of qbits: query tile i's mask row has this key block set (and
             // i is at or below the diagonal when causal); one ballot per 32 tiles
             const uint8_t* m = p.blocks + bh * p.blocks_head_stride;
+            int nch = 1;  // a split plan: this key tile's chunks (its load overlaps the mask loads)
+            if constexpr (SPLIT_) {
+                griddep_wait();
+                nch = p.plan[split_layout(p.plan_tiles, p.plan_help).nchunk + sp_tile];
+            }
             for (int w = 0; w * 32 < n_q; ++w) {
                 const int i = w * 32 + lane;
                 bool u = false;
@@ -335,6 +418,25 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     u = m[static_cast<long long>(i) * p.n_kv + kv_tile] != 0;
                 const uint32_t bits = __ballot_sync(0xffffffffu, u);
                 if (lane == 0) sh.qbits[w] = bits;
+            }
+            if (SPLIT_ && lane == 0) sh.sp_nchunk = nch;
+            // a split tile: keep the chunk's share of the list, the set bits with index
+            // in [chunk c / n, (chunk + 1) c / n)
+            if (nch > 1 && lane == 0) {
+                int c = 0;
+                for (int w = 0; w * 32 < n_q; ++w) c += __popc(sh.qbits[w]);
+                const int lo = sp_chunk * c / nch, hi = (sp_chunk + 1) * c / nch;
+                int seen = 0;
+                for (int w = 0; w * 32 < n_q; ++w) {
+                    uint32_t bits = sh.qbits[w], keep = 0u;
+                    while (bits) {
+                        const uint32_t bit = bits & (0u - bits);
+                        if (seen >= lo && seen < hi) keep |= bit;
+                        ++seen;
+                        bits ^= bit;
+                    }
+                    sh.qbits[w] = keep;
+                }
             }
         }
     }
@@ -795,7 +897,52 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 if (threadIdx.x == 0) bulk_wait_read<0>();
                 named_bar_sync(5, kEW);
             }
-            if (ok) {
+            // A split key tile: this chunk's partial dV and dK (fp32) go to its slot, and
+            // the chunk that finishes last writes dK, dV from the sum of the slots, taken
+            // in chunk order.  (Each chunk writes its slot, fences, then counts itself in;
+            // the last one fences again before it reads the others' slots.)
+            bool store = true;
+            const int nchunks = SPLIT_ ? sh.sp_nchunk : 1;
+            const bool split = SPLIT_ && nchunks > 1;
+            const int tile = SPLIT_ ? sh.sp_tile : 0;
+            const SplitPlan pl = split_layout(p.plan_tiles, p.plan_help);
+            float* part = split ? reinterpret_cast<float*>(p.plan + pl.part) +
+                                      static_cast<size_t>(reinterpret_cast<const uint32_t*>(p.plan + pl.slot)[tile]) *
+                                          2 * 128 * D
+                                : nullptr;
+            if (split) {
+                if (ok) {
+                    tc_fence_after();
+                    float* mine = part + static_cast<size_t>(sh.sp_chunk) * 2 * 128 * D;
+#pragma unroll
+                    for (int which = 0; which < 2; ++which) {
+                        const uint32_t src = tmem + lane_off + (which ? L::kTmDK : L::kTmDV);
+#pragma unroll
+                        for (int cc = 0; cc < kDC; cc += 16) {
+                            const int c0 = h * kDC + cc;
+                            uint32_t o[16];
+                            tmem_ld16(src + c0, o);
+                            tmem_ld_wait(o);
+                            float4* dst4 =
+                                reinterpret_cast<float4*>(mine + (static_cast<size_t>(which) * 128 + r) * D + c0);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                dst4[q] = make_float4(u2f(o[4 * q]), u2f(o[4 * q + 1]), u2f(o[4 * q + 2]),
+                                                      u2f(o[4 * q + 3]));
+                        }
+                    }
+                }
+                __threadfence();
+                named_bar_sync(4, kEW);
+                if (threadIdx.x == 0)
+                    sh.last_chunk =
+                        ok && atomicAdd(reinterpret_cast<unsigned int*>(p.plan + pl.arrive) + tile, 1u) ==
+                                  static_cast<unsigned>(nchunks - 1);
+                named_bar_sync(4, kEW);
+                store = sh.last_chunk != 0;
+                if (store) __threadfence();
+            }
+            if (ok && store) {
                 tc_fence_after();
                 const uint32_t tDV = tmem + lane_off + L::kTmDV, tDK = tmem + lane_off + L::kTmDK;
 #pragma unroll
@@ -807,7 +954,25 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     for (int cc = 0; cc < kDC; cc += 16) {
                         const int c0 = h * kDC + cc;
                         uint32_t o[16];
-                        if (!SPARSE || isteps > 0) {
+                        if (split) {
+                            float f[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) f[i] = 0.f;
+                            for (int c = 0; c < nchunks; ++c) {
+                                const float4* src4 = reinterpret_cast<const float4*>(
+                                    part + ((static_cast<size_t>(c) * 2 + which) * 128 + r) * D + c0);
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    const float4 v = __ldcg(src4 + q);
+                                    f[4 * q] += v.x;
+                                    f[4 * q + 1] += v.y;
+                                    f[4 * q + 2] += v.z;
+                                    f[4 * q + 3] += v.w;
+                                }
+                            }
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(f[i]);
+                        } else if (!SPARSE || isteps > 0) {
                             tmem_ld16(src + c0, o);
                             tmem_ld_wait(o);
                         } else {
@@ -831,7 +996,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                 fence_async_shared();
             }
             named_bar_sync(4, kEW);
-            if (threadIdx.x == 0 && ok) {
+            if (threadIdx.x == 0 && ok && store) {
                 const uint32_t sv = sbase + (PERSIST ? L::kStageKV : L::kV);
                 const uint32_t sk = sbase + (PERSIST ? L::kStageKV + L::kTile : L::kK);
                 for (int b = 0; b < L::kBoxes; ++b) {
@@ -853,6 +1018,177 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+}
+
+// The split plan's inputs: the mask, the plan buffer (the dQ output) and the sizes.
+struct PlanArgs {
+    const uint8_t* blocks;
+    long long head_stride;  // bytes between heads' masks (0: one mask)
+    uint8_t* base;          // the plan buffer, laid out by split_layout
+    int BH, n_kv, n_q, sms, n_help, n_slots, causal;
+};
+
+constexpr int kPlanWarps = kPlanThreads / 32;
+
+__device__ __forceinline__ int block_sum(int v, int* red) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    int t = 0;
+    for (int i = 0; i < kPlanWarps; ++i) t += red[i];
+    return t;
+}
+
+// Exclusive prefix sum over the block of (a, b) pairs, in thread order.
+__device__ __forceinline__ void block_scan2(int& a, int& b, int2* wsum) {
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    int ia = a, ib = b;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int ya = __shfl_up_sync(0xffffffffu, ia, o), yb = __shfl_up_sync(0xffffffffu, ib, o);
+        if (l >= o) {
+            ia += ya;
+            ib += yb;
+        }
+    }
+    __syncthreads();
+    if (l == 31) wsum[w] = make_int2(ia, ib);
+    __syncthreads();
+    if (w == 0) {
+        int2 v = l < kPlanWarps ? wsum[l] : make_int2(0, 0);
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ya = __shfl_up_sync(0xffffffffu, v.x, o), yb = __shfl_up_sync(0xffffffffu, v.y, o);
+            if (l >= o) {
+                v.x += ya;
+                v.y += yb;
+            }
+        }
+        if (l < kPlanWarps) wsum[l] = v;  // inclusive over warps
+    }
+    __syncthreads();
+    const int2 before = w > 0 ? wsum[w - 1] : make_int2(0, 0);
+    a = before.x + ia - a;
+    b = before.y + ib - b;
+}
+
+// Split plan for the block-mask backward: one CTA of kPlanThreads threads.
+// Counts each key tile's query tiles from the mask; takes one SM's share of the
+// work, S = (query tiles + kSplitCtaSteps x key tiles) / SMs, as the chunk length T
+// (at least kSplitMinSteps); splits a key tile of c > 1.5 T query tiles into
+// ceil(c / T) chunks (at most kSplitMaxChunks), doubling T until the helper CTAs
+// and partial slots suffice; and writes per key tile its chunk count and first
+// slot, per helper its (key tile, chunk), zeroed arrival counters, and the number
+// of helper chunks.  Key tiles are numbered in the main kernel's launch order,
+// kt * BH + bh.
+__global__ void __launch_bounds__(kPlanThreads, 1) fa_bwd_plan_kernel(const PlanArgs a) {
+    // the previous kernels on the stream (the D kernel, and the dQ conversion of an
+    // earlier call, which wrote this buffer) are done
+    griddep_wait();
+    __shared__ int red[kPlanWarps];
+    __shared__ int2 wsum[kPlanWarps];
+    const int n_tiles = a.BH * a.n_kv;
+    const SplitPlan pl = split_layout(n_tiles, a.n_help);
+    unsigned int* cnt = reinterpret_cast<unsigned int*>(a.base + pl.cnt);  // [mask head][key tile]
+    const int n_mh = a.head_stride ? a.BH : 1;
+    for (int i = threadIdx.x; i < n_mh * a.n_kv; i += kPlanThreads) cnt[i] = 0u;
+    __syncthreads();
+    // 1. query tiles per key tile.  A thread takes 16 neighbouring key tiles (one
+    //    16-byte piece of a mask row when the rows allow) of one mask head over a
+    //    slice of the query rows and adds its counts in.
+    const int groups = (a.n_kv + 15) / 16;
+    const int G = n_mh * groups;
+    const int S = max(1, kPlanThreads / G);
+    const int R = (a.n_q + S - 1) / S;
+    const bool vec = (reinterpret_cast<uintptr_t>(a.blocks) & 15u) == 0 && (a.n_kv & 15) == 0 &&
+                     (a.head_stride & 15) == 0;
+    for (int u = threadIdx.x; u < G * S; u += kPlanThreads) {
+        const int sl = u / G, g = u - sl * G;
+        const int mh = g / groups, kt0 = (g - mh * groups) * 16;
+        const uint8_t* m = a.blocks + mh * a.head_stride + kt0;
+        const int q0 = sl * R, q1 = min(a.n_q, q0 + R);
+        int c[16];
+#pragma unroll
+        for (int b = 0; b < 16; ++b) c[b] = 0;
+#pragma unroll 4
+        for (int qt = q0; qt < q1; ++qt) {
+            const uint8_t* row = m + static_cast<long long>(qt) * a.n_kv;
+            uint32_t wv[4] = {0u, 0u, 0u, 0u};
+            if (vec) {
+                const uint4 v = *reinterpret_cast<const uint4*>(row);
+                wv[0] = v.x;
+                wv[1] = v.y;
+                wv[2] = v.z;
+                wv[3] = v.w;
+            } else {
+#pragma unroll
+                for (int b = 0; b < 16; ++b)
+                    if (kt0 + b < a.n_kv && row[b] != 0) wv[b >> 2] |= 1u << (8 * (b & 3));
+            }
+#pragma unroll
+            for (int b = 0; b < 16; ++b)  // causal: key tile kt0 + b counts query tiles from the diagonal
+                c[b] += ((wv[b >> 2] >> (8 * (b & 3))) & 0xffu) != 0u && (!a.causal || qt >= kt0 + b);
+        }
+#pragma unroll
+        for (int b = 0; b < 16; ++b)
+            if (kt0 + b < a.n_kv && c[b] != 0) atomicAdd(cnt + mh * a.n_kv + kt0 + b, static_cast<unsigned>(c[b]));
+    }
+    __syncthreads();
+    auto count = [&](int t) {
+        const int kt = t / a.BH, bh = t - kt * a.BH;
+        return static_cast<int>(__ldcg(cnt + (a.head_stride ? bh : 0) * a.n_kv + kt));
+    };
+    // this thread's share of the tiles in launch order: [t0, t1)
+    const int per = (n_tiles + kPlanThreads - 1) / kPlanThreads;
+    const int t0 = min(n_tiles, static_cast<int>(threadIdx.x) * per), t1 = min(n_tiles, t0 + per);
+    int local = 0;
+    for (int t = t0; t < t1; ++t) local += count(t);
+    const long long work = static_cast<long long>(block_sum(local, red)) + static_cast<long long>(kSplitCtaSteps) * n_tiles;
+    // 2. chunk length
+    int T = static_cast<int>(max(static_cast<long long>(kSplitMinSteps), (work + a.sms - 1) / a.sms));
+    auto chunks = [&](int c) { return 2 * c > 3 * T ? min(kSplitMaxChunks, (c + T - 1) / T) : 1; };
+    int need_h = 0, need_s = 0;
+    for (int it = 0; it < 16; ++it) {
+        int h = 0, sl = 0;
+        for (int t = t0; t < t1; ++t) {
+            const int k = chunks(count(t));
+            h += k - 1;
+            sl += k > 1 ? k : 0;
+        }
+        need_h = block_sum(h, red);
+        need_s = block_sum(sl, red);
+        if (need_h <= a.n_help && need_s <= a.n_slots) break;
+        T *= 2;
+    }
+    if (need_h > a.n_help || need_s > a.n_slots) T = 1 << 28;  // no split at all
+    // 3. exclusive prefix sums of helpers and slots in launch order
+    int he = 0, se = 0;
+    for (int t = t0; t < t1; ++t) {
+        const int k = chunks(count(t));
+        he += k - 1;
+        se += k > 1 ? k : 0;
+    }
+    const int my_h = he;
+    block_scan2(he, se, wsum);
+    if (threadIdx.x == kPlanThreads - 1) *reinterpret_cast<uint32_t*>(a.base + pl.hdr) = static_cast<uint32_t>(he + my_h);
+    // 4. the plan
+    uint8_t* nchunk = a.base + pl.nchunk;
+    uint32_t* slot = reinterpret_cast<uint32_t*>(a.base + pl.slot);
+    uint32_t* help = reinterpret_cast<uint32_t*>(a.base + pl.help);
+    unsigned int* arrive = reinterpret_cast<unsigned int*>(a.base + pl.arrive);
+    for (int t = t0; t < t1; ++t) {
+        const int k = chunks(count(t));
+        nchunk[t] = static_cast<uint8_t>(k);
+        slot[t] = static_cast<uint32_t>(se);
+        arrive[t] = 0u;
+        for (int c = 1; c < k; ++c, ++he) {
+            help[2 * he] = static_cast<uint32_t>(t);
+            help[2 * he + 1] = static_cast<uint32_t>(c);
+        }
+        se += k > 1 ? k : 0;
+    }
+    // the main kernel, launched next as a dependent, reads the plan after its own wait
+    griddep_launch_dependents();
 }
 
 // D_i = dO_i . O_i in fp32 and a zeroed dQ accumulator row; D/8 threads per row,
@@ -910,6 +1246,7 @@ __global__ void __launch_bounds__(256) fa_bwd_post_kernel(const float* __restric
     }
 }
 
+
 // Heads per launch-order group (a power of two, at most 16).  Measured on
 // GB300, interleaved runs: causal problems do best with the group's Q, dO, K, V
 // (bf16) and fp32 dQ accumulator near 128 MB (16k tokens, d = 128: 4 heads,
@@ -930,6 +1267,44 @@ template <int D, bool CAUSAL, int MASK = kMaskNone>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     using L = BwdLayout<D>;
     const int64_t rows = static_cast<int64_t>(a.BH) * a.N;
+    // d = 128: four elementwise warpgroups (32 query columns each); d = 64: two
+    // (four measured 4-8% slower there)
+    constexpr int NWG = D == 128 ? 4 : 2;
+    // short d = 64 problems without a mask, with more work items than SMs: the
+    // persistent kernel, so that one item's set-up, first loads and epilogue
+    // overlap the next's
+    constexpr bool kCanPersist = D == 64 && MASK == kMaskNone;
+    int sms = 0;
+    if (kCanPersist || MASK == kMaskBlocks) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cudaGetLastError();
+    }
+    const int n_kv = (a.N + kBK - 1) / kBK;
+    // A block mask with few key tiles per SM: the split plan and the partial slots,
+    // laid out in the dQ output (written only by the dQ conversion kernel, after the
+    // main kernel); one helper CTA per SM
+    PlanArgs pa{};
+    const long long n_tiles = static_cast<long long>(a.BH) * n_kv;
+    if (MASK == kMaskBlocks && a.dQ && n_tiles <= static_cast<long long>(kSplitTilesPerSm) * sms) {
+        const SplitPlan pl = split_layout(static_cast<int>(n_tiles), sms);
+        const size_t dq_bytes = static_cast<size_t>(a.BH) * a.N * D * 2;
+        const size_t slot_bytes = static_cast<size_t>(2) * 128 * D * 4;
+        const long long n_slots = pl.part < dq_bytes ? static_cast<long long>((dq_bytes - pl.part) / slot_bytes) : 0;
+        if (n_slots >= 2) {
+            pa.blocks = a.blocks;
+            pa.head_stride = a.blocks_head_stride;
+            pa.base = static_cast<uint8_t*>(a.dQ);
+            pa.BH = a.BH;
+            pa.n_kv = n_kv;
+            pa.n_q = (a.N + kBQ - 1) / kBQ;
+            pa.sms = sms;
+            pa.n_help = sms;
+            pa.n_slots = static_cast<int>(std::min<long long>(n_slots, 1ll << 30));
+            pa.causal = CAUSAL;
+        }
+    }
     // 1. D and a zeroed accumulator
     {
         constexpr int TPR = D / 8;
@@ -952,32 +1327,20 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
             !make_tile_map(&tdk, a.dK, BF, 2, D, a.N, a.BH, 64, kBK) ||
             !make_tile_map(&tdv, a.dV, BF, 2, D, a.N, a.BH, 64, kBK))
             return cudaErrorInvalidValue;
-        // d = 128: four elementwise warpgroups (32 query columns each); d = 64: two
-        // (four measured 4-8% slower there)
-        constexpr int NWG = D == 128 ? 4 : 2;
-        // short d = 64 problems without a mask, with more work items than SMs: the
-        // persistent kernel, so that one item's set-up, first loads and epilogue
-        // overlap the next's
-        constexpr bool kCanPersist = D == 64 && MASK == kMaskNone;
-        int sms = 0;
-        if (kCanPersist) {
-            int dev = 0;
-            if (cudaGetDevice(&dev) != cudaSuccess ||
-                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-                return cudaGetLastError();
-        }
         const long long items = static_cast<long long>(a.BH) * ((a.N + kBK - 1) / kBK);
         const bool persist = kCanPersist && a.N <= kBwdPersistMaxN && items > sms;
         constexpr auto kern = &fa_bwd_main_kernel<D, CAUSAL, MASK, NWG>;
         constexpr auto kern_p = &fa_bwd_main_kernel<D, CAUSAL, MASK, NWG, kCanPersist>;
-        cudaError_t e = persist ? set_max_dyn_smem_once<kern_p>(L::kBytesPersist)
-                                : set_max_dyn_smem_once<kern>(L::kBytes);
+        constexpr auto kern_s = &fa_bwd_main_kernel<D, CAUSAL, MASK, NWG, false, MASK == kMaskBlocks>;
+        cudaError_t e = persist   ? set_max_dyn_smem_once<kern_p>(L::kBytesPersist)
+                        : pa.base ? set_max_dyn_smem_once<kern_s>(L::kBytes)
+                                  : set_max_dyn_smem_once<kern>(L::kBytes);
         if (e != cudaSuccess) return e;
         BwdParams p;
         p.LSE = a.LSE;
         p.Dvec = a.D;
         p.N = a.N;
-        p.n_kv = (a.N + kBK - 1) / kBK;
+        p.n_kv = n_kv;
         p.scale_log2 = a.tau * kLog2e;
         p.tau = a.tau;
         p.window = (a.window > 0 && a.window < a.N) ? a.window : 0;
@@ -989,13 +1352,25 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         p.BH = a.BH;
         if (items > (1ll << 30)) return cudaErrorInvalidValue;
         p.items = static_cast<int>(items);
+        p.plan = nullptr;
+        p.plan_tiles = p.plan_help = 0;
         dim3 grid(static_cast<unsigned>(a.BH), static_cast<unsigned>(p.n_kv));
         if (persist) grid = dim3(static_cast<unsigned>(sms));
         if (a.ev_start) cudaEventRecord(a.ev_start, stream);
-        e = persist ? launch_dependent(kern_p, grid, dim3(bwd_threads(NWG)), L::kBytesPersist, stream, tq, tk,
-                                       tv, tdo, tacc, tdk, tdv, p)
-                    : launch_dependent(kern, grid, dim3(bwd_threads(NWG)), L::kBytes, stream, tq, tk, tv, tdo,
-                                       tacc, tdk, tdv, p);
+        if (pa.base) {
+            e = launch_dependent(fa_bwd_plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, pa);
+            if (e != cudaSuccess) return e;
+            p.plan = pa.base;
+            p.plan_tiles = static_cast<int>(n_tiles);
+            p.plan_help = pa.n_help;
+            grid = dim3(static_cast<unsigned>(n_tiles + pa.n_help));
+        }
+        e = persist   ? launch_dependent(kern_p, grid, dim3(bwd_threads(NWG)), L::kBytesPersist, stream, tq, tk,
+                                         tv, tdo, tacc, tdk, tdv, p)
+            : pa.base ? launch_dependent(kern_s, grid, dim3(bwd_threads(NWG)), L::kBytes, stream, tq, tk, tv, tdo,
+                                         tacc, tdk, tdv, p)
+                      : launch_dependent(kern, grid, dim3(bwd_threads(NWG)), L::kBytes, stream, tq, tk, tv, tdo,
+                                         tacc, tdk, tdv, p);
         if (e == cudaSuccess && a.ev_stop) e = cudaEventRecord(a.ev_stop, stream);
         if (e != cudaSuccess) return e;
     }

@@ -180,7 +180,9 @@ FA_API fa_status fa_fwd_blocks(const void* Q, const void* K, const void* V, void
  * Block-sparse backward: fa_bwd for the mask of fa_fwd_blocks (LSE must come
  * from fa_fwd_blocks with the same mask).  Rows that see no key get dQ = 0;
  * keys that no query sees get dK = dV = 0.  Same workspace rules as fa_bwd;
- * the mask must not overlap dQ, dK, dV or the workspace.
+ * the mask must not overlap dQ, dK, dV or the workspace.  Until its last
+ * kernel writes dQ, the call keeps in dQ's memory the plan that splits key
+ * tiles seen by many query tiles over extra CTAs, and their partial dK, dV.
  */
 FA_API fa_status fa_bwd_blocks(const void* Q, const void* K, const void* V, const void* O,
                                const void* dO, const float* LSE, void* dQ, void* dK, void* dV,

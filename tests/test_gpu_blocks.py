@@ -88,6 +88,38 @@ def test_all_ones_mask_is_the_dense_kernel_bitwise(causal):
     assert (g[0].float() - g0[0].float()).abs().max().item() <= 1e-2
 
 
+# Key tiles visited by many query tiles (here the two global anchors, seen by all
+# 32 query tiles) are split into chunks that extra CTAs run; the last chunk to
+# finish adds the partial dK, dV in chunk order.
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_split_key_tiles_match_oracle(causal, d):
+    B, H, N = 1, 2, 4096
+    x = draw(B, H, N, d, seed=61 + d + int(causal))
+    nb = nblocks(N)
+    mask = local_global_block_mask(nb, local=2, anchors=2, heads=B * H, extra=0.01, seed=9)
+    tau = 1 / math.sqrt(d)
+    o, lse, (dq, dk, dv) = gpu(x, causal, tau, mask.reshape(B, H, nb, nb))
+    o_ref, l_ref = oracle.fwd(x["q"], x["k"], x["v"], tau, causal, blocks=mask, blk=EDGE)
+    check_fwd(o, lse, o_ref, l_ref)
+    rq, rk, rv = oracle.bwd(x["q"], x["k"], x["v"], x["do"], tau, causal, blocks=mask, blk=EDGE)
+    check_grad(dq, rq, "dQ")
+    check_grad(dk, rk, "dK")
+    check_grad(dv, rv, "dV")
+
+
+def test_split_key_tiles_are_deterministic():
+    """The split key tiles' dK and dV do not depend on which chunk finishes last:
+    two runs agree bit for bit."""
+    B, H, N, d = 1, 4, 4096, 128
+    x = draw(B, H, N, d, seed=66)
+    nb = nblocks(N)
+    mask = local_global_block_mask(nb, local=2, anchors=2, heads=B * H, seed=10)
+    a = gpu(x, True, 0.09, mask.reshape(B, H, nb, nb))
+    b = gpu(x, True, 0.09, mask.reshape(B, H, nb, nb))
+    assert torch.equal(a[2][1], b[2][1]) and torch.equal(a[2][2], b[2][2])
+
+
 def test_shared_mask_equals_the_same_mask_per_head_bitwise():
     N, d, B, H = 520, 64, 2, 3
     x = draw(B, H, N, d, seed=32)
