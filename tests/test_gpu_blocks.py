@@ -108,6 +108,22 @@ def test_split_key_tiles_match_oracle(causal, d):
     check_grad(dv, rv, "dV")
 
 
+def test_split_with_a_shared_mask_and_ragged_rows():
+    """One mask for every head (the plan counts it once), 26 query tiles with a
+    ragged last one, and rows of 26 mask bytes (the plan's byte-wise path): the
+    anchors' 26 and 25 query tiles are split in two."""
+    B, H, N, d = 1, 2, 3300, 128
+    x = draw(B, H, N, d, seed=67)
+    nb = nblocks(N)
+    mask = local_global_block_mask(nb, local=2, anchors=2, heads=1, seed=11)[0]
+    tau = 1 / math.sqrt(d)
+    o, lse, (dq, dk, dv) = gpu(x, True, tau, mask)
+    rq, rk, rv = oracle.bwd(x["q"], x["k"], x["v"], x["do"], tau, True, blocks=mask, blk=EDGE)
+    check_grad(dq, rq, "dQ")
+    check_grad(dk, rk, "dK")
+    check_grad(dv, rv, "dV")
+
+
 def test_split_key_tiles_are_deterministic():
     """The split key tiles' dK and dV do not depend on which chunk finishes last:
     two runs agree bit for bit."""
