@@ -15,6 +15,7 @@ data-path collective, only a barrier and a max over ranks for timing.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -590,9 +591,19 @@ def measure_blocks(w, q, k, v, do, dev, steps, peak):
     ff = blocks_flops_fwd(B, H, N, d, True, m)
     dense = 4.0 * B * H * N * N * d / 2
     mt = torch.from_numpy(m).to(dev).reshape(B, H, nb, nb)
-    return {"mask": "per head: 4 local + 2 anchor blocks of 128, 2% random extra (seed 3)",
-            "causal_work_fraction": round(ff / dense, 4),
-            **measure_variant(w, q, k, v, do, dev, steps, peak, ff, blocks=mt)}
+    out = {"mask": "per head: 4 local + 2 anchor blocks of 128, 2% random extra (seed 3)",
+           "causal_work_fraction": round(ff / dense, 4),
+           **measure_variant(w, q, k, v, do, dev, steps, peak, ff, blocks=mt)}
+    # the first two heads alone: few key tiles per SM, where the backward splits the
+    # anchor key tiles (seen by every query tile) over helper CTAs
+    if B * H > 2:
+        w2 = dataclasses.replace(w, B=1, H=2)
+        sl = [t.reshape(B * H, N, d)[:2].reshape(1, 2, N, d).contiguous() for t in (q, k, v, do)]
+        f2 = blocks_flops_fwd(1, 2, N, d, True, m[:2])
+        out["two_heads"] = {"shape": [1, 2, N, d], **measure_variant(w2, *sl, dev, steps, peak, f2,
+                                                                     blocks=mt.reshape(B * H, nb, nb)[:2]
+                                                                     .reshape(1, 2, nb, nb).contiguous())}
+    return out
 
 
 def measure_decode(dev, steps, peaks, shape=None):
