@@ -85,8 +85,8 @@ constexpr int kPlanThreads = 1024;
 // helper chunks in use (u32); per key tile in launch order kt * BH + bh its chunk
 // count (u8, 1: not split), first partial slot (u32) and finished chunks (u32);
 // per helper CTA its (key tile, chunk) (2 x u32); the planner's query-tile counts
-// per mask head and key tile (u32); then the partial slots, each [dV, dK][128
-// keys][D] fp32.
+// per mask head and key tile (u32); then the partial slots, each [dV, dK][D / 4]
+// [128 keys][4] fp32 (a warp's 32 key rows of four columns are contiguous).
 struct SplitPlan {
     size_t hdr, nchunk, slot, help, arrive, cnt, part;
 };
@@ -923,12 +923,14 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                             uint32_t o[16];
                             tmem_ld16(src + c0, o);
                             tmem_ld_wait(o);
-                            float4* dst4 =
-                                reinterpret_cast<float4*>(mine + (static_cast<size_t>(which) * 128 + r) * D + c0);
+                            // slot layout [dV, dK][column / 4][key row][4]: a warp's 32 rows
+                            // of one float4 column group are 512 contiguous bytes
+                            float4* dst4 = reinterpret_cast<float4*>(mine + static_cast<size_t>(which) * 128 * D) +
+                                           (c0 / 4) * 128 + r;
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
-                                dst4[q] = make_float4(u2f(o[4 * q]), u2f(o[4 * q + 1]), u2f(o[4 * q + 2]),
-                                                      u2f(o[4 * q + 3]));
+                                dst4[q * 128] = make_float4(u2f(o[4 * q]), u2f(o[4 * q + 1]), u2f(o[4 * q + 2]),
+                                                            u2f(o[4 * q + 3]));
                         }
                     }
                 }
@@ -955,19 +957,38 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                         const int c0 = h * kDC + cc;
                         uint32_t o[16];
                         if (split) {
+                            // 8 columns of every chunk's slot in flight at once (the slots
+                            // were written by other SMs, possibly on the other die), then
+                            // added in chunk order; each load instruction reads 512
+                            // contiguous bytes
                             float f[16];
 #pragma unroll
                             for (int i = 0; i < 16; ++i) f[i] = 0.f;
-                            for (int c = 0; c < nchunks; ++c) {
-                                const float4* src4 = reinterpret_cast<const float4*>(
-                                    part + ((static_cast<size_t>(c) * 2 + which) * 128 + r) * D + c0);
 #pragma unroll
-                                for (int q = 0; q < 4; ++q) {
-                                    const float4 v = __ldcg(src4 + q);
-                                    f[4 * q] += v.x;
-                                    f[4 * q + 1] += v.y;
-                                    f[4 * q + 2] += v.z;
-                                    f[4 * q + 3] += v.w;
+                            for (int hq = 0; hq < 2; ++hq) {
+                                float4 v[kSplitMaxChunks][2];
+#pragma unroll
+                                for (int c = 0; c < kSplitMaxChunks; ++c) {
+                                    if (c < nchunks) {
+                                        const float4* src4 =
+                                            reinterpret_cast<const float4*>(
+                                                part + (static_cast<size_t>(c) * 2 + which) * 128 * D) +
+                                            (c0 / 4 + 2 * hq) * 128 + r;
+                                        v[c][0] = __ldcg(src4);
+                                        v[c][1] = __ldcg(src4 + 128);
+                                    }
+                                }
+#pragma unroll
+                                for (int c = 0; c < kSplitMaxChunks; ++c) {
+                                    if (c < nchunks) {
+#pragma unroll
+                                        for (int e = 0; e < 2; ++e) {
+                                            f[8 * hq + 4 * e] += v[c][e].x;
+                                            f[8 * hq + 4 * e + 1] += v[c][e].y;
+                                            f[8 * hq + 4 * e + 2] += v[c][e].z;
+                                            f[8 * hq + 4 * e + 3] += v[c][e].w;
+                                        }
+                                    }
                                 }
                             }
 #pragma unroll
