@@ -746,6 +746,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                     // most tiles need no mask: the loop is built twice, and the masked
                     // copy runs only on the diagonal, window-edge and ragged-end tiles
                     const bool masked = diag || wedge || kvs + kBK > N;
+                    // this key row's visible query columns q (offsets in the warpgroup's
+                    // slice) are lo <= q < hi: above the diagonal q < kg - qh is hidden,
+                    // past the window edge q >= kg + window - qh, and a key row past a
+                    // ragged end sees none
+                    const int lo = kg >= N ? (1 << 30) : (diag ? kg - qh : -(1 << 30));
+                    const int hi = (LOCAL && wedge) ? kg + window - qh : (1 << 30);
 #pragma unroll
                     for (int c = 0; c < kQC / 32; ++c) {
                         uint32_t sv[32];
@@ -765,17 +771,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                                 float p0 = ex2(x.x);
                                 float p1 = ex2(x.y);
                                 if constexpr (decltype(with_mask)::value) {
-                                    if (diag) {
-                                        if (kg > qh + q) p0 = 0.f;
-                                        if (kg > qh + q + 1) p1 = 0.f;
-                                    }
-                                    if constexpr (LOCAL) {
-                                        if (wedge) {
-                                            if (qh + q >= kg + window) p0 = 0.f;
-                                            if (qh + q + 1 >= kg + window) p1 = 0.f;
-                                        }
-                                    }
-                                    if (kg >= N) p0 = p1 = 0.f;  // key row past a ragged end
+                                    if (q < lo || q >= hi) p0 = 0.f;
+                                    if (q + 1 < lo || q + 1 >= hi) p1 = 0.f;
                                 }
                                 pk[i] = pack_bf16(p0, p1);
                             }
