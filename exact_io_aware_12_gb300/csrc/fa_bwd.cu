@@ -84,11 +84,11 @@ constexpr int kPlanThreads = 1024;
 // The plan's arrays in its buffer (byte offsets, each 256-aligned): the number of
 // helper chunks in use (u32); per key tile in launch order kt * BH + bh its chunk
 // count (u8, 1: not split), first partial slot (u32) and finished chunks (u32);
-// per helper CTA its (key tile, chunk) (2 x u32); the planner's query-tile counts
-// per mask head and key tile (u32); then the partial slots, each [dV, dK][D / 4]
-// [128 keys][4] fp32 (a warp's 32 key rows of four columns are contiguous).
+// per helper CTA its (key tile, chunk) (2 x u32); then the partial slots, each
+// [dV, dK][D / 4][128 keys][4] fp32 (a warp's 32 key rows of four columns are
+// contiguous).
 struct SplitPlan {
-    size_t hdr, nchunk, slot, help, arrive, cnt, part;
+    size_t hdr, nchunk, slot, help, arrive, part;
 };
 __host__ __device__ __forceinline__ SplitPlan split_layout(int n_tiles, int n_help) {
     const auto up = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -98,8 +98,7 @@ __host__ __device__ __forceinline__ SplitPlan split_layout(int n_tiles, int n_he
     s.slot = s.nchunk + up(static_cast<size_t>(n_tiles));
     s.help = s.slot + up(4 * static_cast<size_t>(n_tiles));
     s.arrive = s.help + up(8 * static_cast<size_t>(n_help));
-    s.cnt = s.arrive + up(4 * static_cast<size_t>(n_tiles));
-    s.part = s.cnt + up(4 * static_cast<size_t>(n_tiles));
+    s.part = s.arrive + up(4 * static_cast<size_t>(n_tiles));
     return s;
 }
 
@@ -1105,11 +1104,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) fa_bwd_plan_kernel(const Plan
     griddep_wait();
     __shared__ int red[kPlanWarps];
     __shared__ int2 wsum[kPlanWarps];
-    const int n_tiles = a.BH * a.n_kv;
+    __shared__ unsigned int cnt[kPlanThreads];  // [mask head][key tile]: query tiles
+    const int n_tiles = a.BH * a.n_kv;          // at most kPlanThreads (the launcher's bound)
     const SplitPlan pl = split_layout(n_tiles, a.n_help);
-    unsigned int* cnt = reinterpret_cast<unsigned int*>(a.base + pl.cnt);  // [mask head][key tile]
     const int n_mh = a.head_stride ? a.BH : 1;
-    for (int i = threadIdx.x; i < n_mh * a.n_kv; i += kPlanThreads) cnt[i] = 0u;
+    cnt[threadIdx.x] = 0u;
     __syncthreads();
     // 1. query tiles per key tile.  A thread takes 16 neighbouring key tiles (one
     //    16-byte piece of a mask row when the rows allow) of one mask head over a
@@ -1149,61 +1148,44 @@ __global__ void __launch_bounds__(kPlanThreads, 1) fa_bwd_plan_kernel(const Plan
         }
 #pragma unroll
         for (int b = 0; b < 16; ++b)
-            if (kt0 + b < a.n_kv && c[b] != 0) atomicAdd(cnt + mh * a.n_kv + kt0 + b, static_cast<unsigned>(c[b]));
+            if (kt0 + b < a.n_kv && c[b] != 0) atomicAdd(&cnt[mh * a.n_kv + kt0 + b], static_cast<unsigned>(c[b]));
     }
     __syncthreads();
-    auto count = [&](int t) {
+    // thread t plans key tile t (launch order kt * BH + bh)
+    const int t = static_cast<int>(threadIdx.x);
+    int my = 0;
+    if (t < n_tiles) {
         const int kt = t / a.BH, bh = t - kt * a.BH;
-        return static_cast<int>(__ldcg(cnt + (a.head_stride ? bh : 0) * a.n_kv + kt));
-    };
-    // this thread's share of the tiles in launch order: [t0, t1)
-    const int per = (n_tiles + kPlanThreads - 1) / kPlanThreads;
-    const int t0 = min(n_tiles, static_cast<int>(threadIdx.x) * per), t1 = min(n_tiles, t0 + per);
-    int local = 0;
-    for (int t = t0; t < t1; ++t) local += count(t);
-    const long long work = static_cast<long long>(block_sum(local, red)) + static_cast<long long>(kSplitCtaSteps) * n_tiles;
+        my = static_cast<int>(cnt[(a.head_stride ? bh : 0) * a.n_kv + kt]);
+    }
+    const long long work = static_cast<long long>(block_sum(my, red)) + static_cast<long long>(kSplitCtaSteps) * n_tiles;
     // 2. chunk length
     int T = static_cast<int>(max(static_cast<long long>(kSplitMinSteps), (work + a.sms - 1) / a.sms));
     auto chunks = [&](int c) { return 2 * c > 3 * T ? min(kSplitMaxChunks, (c + T - 1) / T) : 1; };
     int need_h = 0, need_s = 0;
     for (int it = 0; it < 16; ++it) {
-        int h = 0, sl = 0;
-        for (int t = t0; t < t1; ++t) {
-            const int k = chunks(count(t));
-            h += k - 1;
-            sl += k > 1 ? k : 0;
-        }
-        need_h = block_sum(h, red);
-        need_s = block_sum(sl, red);
+        const int k = chunks(my);
+        need_h = block_sum(k - 1, red);
+        need_s = block_sum(k > 1 ? k : 0, red);
         if (need_h <= a.n_help && need_s <= a.n_slots) break;
         T *= 2;
     }
     if (need_h > a.n_help || need_s > a.n_slots) T = 1 << 28;  // no split at all
     // 3. exclusive prefix sums of helpers and slots in launch order
-    int he = 0, se = 0;
-    for (int t = t0; t < t1; ++t) {
-        const int k = chunks(count(t));
-        he += k - 1;
-        se += k > 1 ? k : 0;
-    }
-    const int my_h = he;
+    const int k = chunks(my);
+    int he = k - 1, se = k > 1 ? k : 0;
     block_scan2(he, se, wsum);
-    if (threadIdx.x == kPlanThreads - 1) *reinterpret_cast<uint32_t*>(a.base + pl.hdr) = static_cast<uint32_t>(he + my_h);
+    if (t == kPlanThreads - 1) *reinterpret_cast<uint32_t*>(a.base + pl.hdr) = static_cast<uint32_t>(he + k - 1);
     // 4. the plan
-    uint8_t* nchunk = a.base + pl.nchunk;
-    uint32_t* slot = reinterpret_cast<uint32_t*>(a.base + pl.slot);
-    uint32_t* help = reinterpret_cast<uint32_t*>(a.base + pl.help);
-    unsigned int* arrive = reinterpret_cast<unsigned int*>(a.base + pl.arrive);
-    for (int t = t0; t < t1; ++t) {
-        const int k = chunks(count(t));
-        nchunk[t] = static_cast<uint8_t>(k);
-        slot[t] = static_cast<uint32_t>(se);
-        arrive[t] = 0u;
+    if (t < n_tiles) {
+        a.base[pl.nchunk + t] = static_cast<uint8_t>(k);
+        reinterpret_cast<uint32_t*>(a.base + pl.slot)[t] = static_cast<uint32_t>(se);
+        reinterpret_cast<unsigned int*>(a.base + pl.arrive)[t] = 0u;
+        uint32_t* help = reinterpret_cast<uint32_t*>(a.base + pl.help);
         for (int c = 1; c < k; ++c, ++he) {
             help[2 * he] = static_cast<uint32_t>(t);
             help[2 * he + 1] = static_cast<uint32_t>(c);
         }
-        se += k > 1 ? k : 0;
     }
     // the main kernel, launched next as a dependent, reads the plan after its own wait
     griddep_launch_dependents();
@@ -1305,7 +1287,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
     // main kernel); one helper CTA per SM
     PlanArgs pa{};
     const long long n_tiles = static_cast<long long>(a.BH) * n_kv;
-    if (MASK == kMaskBlocks && a.dQ && n_tiles <= static_cast<long long>(kSplitTilesPerSm) * sms) {
+    if (MASK == kMaskBlocks && a.dQ && n_tiles <= std::min<long long>(static_cast<long long>(kSplitTilesPerSm) * sms,
+                                                                    kPlanThreads)) {
         const SplitPlan pl = split_layout(static_cast<int>(n_tiles), sms);
         const size_t dq_bytes = static_cast<size_t>(a.BH) * a.N * D * 2;
         const size_t slot_bytes = static_cast<size_t>(2) * 128 * D * 4;
